@@ -1,0 +1,181 @@
+/*
+ * moe_fp8.h - C ABI of the routed FP8 Mixture-of-Experts FFN forward for
+ * sm_103a (GB300).
+ *
+ * The layer (Kimi K2 MoE block FFN):
+ *   scores  s = sigmoid(x W_g^T)                    "Kimi-K2-Base", Mixture of experts: Router score
+ *   choice  c = s + b  (bias used only to choose)    same section: Load balancing (e_score_correction_bias)
+ *   I       = top-k of c per token (one group)       same section: Experts per token, Group-limited routing none
+ *   w_j     = s_{I_j} / sum_j s_{I_j} * 2.827        same section: Renormalize top-k, Routed scaling factor
+ *   E_e(x)  = down(silu(gate x) * up x), no bias     "Kimi-K2-Base", Feed-forward: Activation, FFN bias
+ *   y       = shared(x) + sum_j w_j E_{I_j}(x)       "Kimi K2 · Architecture", Fact sheet: 384 routed + 1 shared
+ * Weights are e4m3 with one fp32 scale per 128x128 block ("Kimi K2 ·
+ * Architecture", config.json quantization_config); activations entering each
+ * projection are quantised dynamically to e4m3 in 1x128 groups with an fp32
+ * scale amax/448 ("Kimi-K2-Base", Pretraining recipe: Training precision).
+ *
+ * Conventions for every call:
+ *  - Memory: every pointer is DEVICE memory allocated and owned by the caller,
+ *    except `cfg` (host). The library never allocates or frees and never
+ *    synchronises the stream. Device buffers must be 16-byte aligned.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream). Every
+ *    call only enqueues work on it and returns.
+ *  - Errors: every call returns a moe_status_t. Arguments are checked on the
+ *    host before anything is enqueued; on an error nothing is enqueued.
+ *    moe_last_error_string() describes the last error of the calling thread.
+ *  - T = 0 is legal for every call and enqueues nothing.
+ *  - Layouts are row-major. Weight matrices use the nn.Linear layout
+ *    [out_features, in_features]. Scales of 1x128 activation groups are stored
+ *    K-block-major ("transposed"): scale of row r, group g at [g * rows + r]
+ *    unless a call says otherwise.
+ *  - Shapes: d and H multiples of 128; 1 <= topk <= 32, topk <= E <= 1024;
+ *    0 <= n_shared <= 4.
+ */
+#ifndef MOE_FP8_H
+#define MOE_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = -1,          /* null pointer, misaligned pointer, bad size or short workspace */
+    MOE_ERR_UNSUPPORTED = -2,  /* shape outside the supported range */
+    MOE_ERR_CUDA = -3,         /* a CUDA call or launch failed; see moe_last_error_string() */
+    MOE_ERR_TIMEOUT = -4       /* a bounded device wait gave up (reported by moe_check_device_error) */
+} moe_status_t;
+
+/* Shape of one MoE layer. */
+typedef struct {
+    int d;              /* model width (hidden_size) */
+    int E;              /* routed experts (n_routed_experts) */
+    int topk;           /* experts chosen per token (num_experts_per_tok) */
+    int H;              /* hidden features of one expert (moe_intermediate_size) */
+    int n_shared;       /* always-on shared experts (n_shared_experts) */
+    float route_scale;  /* routed_scaling_factor */
+} moe_cfg_t;
+
+/* Rows of the permuted activation buffer: topk*T routed rows, then n_shared*T
+ * shared-expert rows (row topk*T + s*T + t holds token t for shared expert s). */
+int64_t moe_permuted_rows(const moe_cfg_t *cfg, int T);
+
+/* Bytes of caller-provided workspace needed by moe_route, moe_permute,
+ * moe_expert_gemm_fp8 and moe_layer_forward for T tokens (one size fits all
+ * of them). Returns 0 for an invalid cfg. Host only. */
+size_t moe_workspace_bytes(const moe_cfg_t *cfg, int T);
+
+/* Dynamic 1x128 quantisation ("Kimi-K2-Base", Pretraining recipe: Training
+ * precision; scale = amax / 448).
+ * in      [rows, cols] bf16 (in_is_bf16 = 1) or fp32 (in_is_bf16 = 0)
+ * q       [rows, cols] e4m3 codes (uint8)
+ * s       [rows, cols/128] fp32, ROW-major (s_transposed = 0) or
+ *         [cols/128, rows] (s_transposed = 1)
+ * Per group of 128 columns: s = fp32(amax) / 448 (IEEE division);
+ * q = e4m3(fp32(x) / s) (IEEE division, round to nearest even, saturate to
+ * +-448); a group with amax = 0 gets s = 0 and codes 0x00. cols % 128 == 0. */
+int moe_quant_fp8_1x128(const void *in, int in_is_bf16, int64_t rows, int cols,
+                        uint8_t *q, float *s, int s_transposed, void *stream);
+
+/* Router ("Kimi-K2-Base", Mixture of experts: Router score, Load balancing,
+ * Renormalize top-k, Routed scaling factor).
+ * x         [T, d] bf16;  w_gate [E, d] bf16;  bias [E] fp32
+ * topk_idx  [T, topk] int32: chosen experts, descending biased score, equal
+ *           scores ordered by the lower expert id
+ * topk_w    [T, topk] fp32: s_I / sum(s_I) * route_scale (unbiased scores)
+ * scores    [T, E] fp32 sigmoid scores, or NULL
+ * Logits accumulate in fp32 on the tensor cores; sigmoid, bias and weights in fp32. */
+int moe_route(const void *x, const void *w_gate, const float *bias, const moe_cfg_t *cfg, int T,
+              int32_t *topk_idx, float *topk_w, float *scores,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Token permutation into contiguous per-expert segments (deterministic).
+ * topk_idx   [T, topk] int32 (each row distinct ids < E)
+ * xq, sx     [T, d] e4m3 and [T, d/128] fp32 ROW-major (moe_quant_fp8_1x128, s_transposed = 0)
+ * offsets    [E + 1] int32: exclusive prefix sum of per-expert counts, offsets[E] = topk*T
+ * sorted_tok [topk*T] int32: segment e = [offsets[e], offsets[e+1]) holds its tokens ascending
+ * inv_pos    [T, topk] int32: position of assignment (t, topk_idx[t, j]) in sorted_tok
+ * xq_perm    [moe_permuted_rows, d] e4m3: row p < topk*T is xq[sorted_tok[p]];
+ *            then n_shared copies of xq in token order
+ * sx_perm    [d/128, moe_permuted_rows] fp32 (K-block-major) scales of xq_perm's rows */
+int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx,
+                const moe_cfg_t *cfg, int T,
+                int32_t *offsets, int32_t *sorted_tok, int32_t *inv_pos,
+                uint8_t *xq_perm, float *sx_perm,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Grouped expert SwiGLU over FP8 weights ("Kimi-K2-Base", Feed-forward):
+ * for each expert segment, o = down(silu(gate x) * up x), with h = silu(g) * u
+ * quantised 1x128 between the two projections. Runs on the tcgen05 tensor
+ * cores; the 128x128 weight scales and the 1x128 activation scales are applied
+ * per 128-wide K block in fp32.
+ * xq_perm, sx_perm  as written by moe_permute; offsets [E+1] (device)
+ * w13    [E+S, 2, H, d] e4m3 (index 0 gate_proj, 1 up_proj); w13_s [E+S, 2, H/128, d/128] fp32
+ * w2     [E+S, d, H] e4m3 (down_proj); w2_s [E+S, d/128, H/128] fp32
+ * o      [moe_permuted_rows, d] bf16, same row order as xq_perm
+ * Routed experts come first, shared experts last. */
+int moe_expert_gemm_fp8(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets,
+                        const uint8_t *w13, const float *w13_s, const uint8_t *w2, const float *w2_s,
+                        const moe_cfg_t *cfg, int T, void *o,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* The two halves of moe_expert_gemm_fp8, for callers that schedule them apart.
+ * moe_expert_gateup_fp8: h = silu(gate x) * up x per expert segment, quantised 1x128:
+ *   hq [moe_permuted_rows, H] e4m3, hs [H/128, moe_permuted_rows] fp32 (K-block-major).
+ * moe_expert_down_fp8: o = down(h) per expert segment from hq/hs; o as in moe_expert_gemm_fp8.
+ * Other arguments as in moe_expert_gemm_fp8. */
+int moe_expert_gateup_fp8(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets,
+                          const uint8_t *w13, const float *w13_s, const moe_cfg_t *cfg, int T,
+                          uint8_t *hq, float *hs, void *workspace, size_t workspace_bytes, void *stream);
+int moe_expert_down_fp8(const uint8_t *hq, const float *hs, const int32_t *offsets,
+                        const uint8_t *w2, const float *w2_s, const moe_cfg_t *cfg, int T, void *o,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Weighted combine: y[t] = sum_s o[topk*T + s*T + t] + sum_j topk_w[t, j] * o[inv_pos[t, j]],
+ * in fp32 in that order, rounded to bf16.
+ * o [moe_permuted_rows, d] bf16; topk_w, inv_pos [T, topk]; y [T, d] bf16. */
+int moe_combine(const void *o, const float *topk_w, const int32_t *inv_pos,
+                const moe_cfg_t *cfg, int T, void *y, void *stream);
+
+/* The whole layer: route, quantise x, permute, grouped expert GEMMs, combine.
+ * x [T, d] bf16; w_gate [E, d] bf16; bias [E] fp32; weights as in
+ * moe_expert_gemm_fp8; y [T, d] bf16. topk_idx / topk_w [T, topk] receive the
+ * routing when not NULL. workspace: moe_workspace_bytes(cfg, T) bytes. */
+int moe_layer_forward(const void *x, const void *w_gate, const float *bias,
+                      const uint8_t *w13, const float *w13_s, const uint8_t *w2, const float *w2_s,
+                      const moe_cfg_t *cfg, int T, void *y, int32_t *topk_idx, float *topk_w,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace for dense_swiglu_fp8. Host only. */
+size_t dense_swiglu_workspace_bytes(int d, int H, int T);
+
+/* Dense SwiGLU FFN of the first block ("Kimi K2 · Dense transformer block",
+ * Parameters: SwiGLU MLP; "Kimi K2 · Architecture", config.json
+ * intermediate_size): y = down(silu(gate x) * up x) with FP8 weights,
+ * x and h quantised 1x128.
+ * x [T, d] bf16; w13 [2, H, d] e4m3, w13_s [2, H/128, d/128]; w2 [d, H] e4m3,
+ * w2_s [d/128, H/128]; y [T, d] bf16. */
+int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s,
+                     const uint8_t *w2, const float *w2_s, int d, int H, int T, void *y,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Reads and clears the device error word of the current device after
+ * synchronising `stream`. MOE_ERR_TIMEOUT if a kernel's bounded wait on an
+ * mbarrier gave up since the last check (its outputs are then invalid);
+ * MOE_OK otherwise. *detail (may be NULL) receives the raw error bits. */
+int moe_check_device_error(void *stream, uint32_t *detail);
+
+/* Description of the calling thread's last error (static storage). */
+const char *moe_last_error_string(void);
+
+/* Number of kernels the last successful call enqueued (calling thread). */
+int moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP8_H */

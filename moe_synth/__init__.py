@@ -150,21 +150,31 @@ class ExpertWeights:
                 self.w2[e], self.w2_s[e])
 
 
+def gen_expert(e: int, d: int, H: int, seed: int = 0, device="cpu", std: float = 0.02, name: str = "expert"):
+    """Expert e's weights: (w13 uint8 [2, H, d], w13_s [2, H/128, d/128], w2 uint8 [d, H], w2_s [d/128, H/128]).
+
+    Each matrix has its own seed, so one expert can be regenerated alone."""
+    q1, s1 = fp8_blocks(randn((H, d), std, device, seed, f"{name}.w1", e))
+    q3, s3 = fp8_blocks(randn((H, d), std, device, seed, f"{name}.w3", e))
+    q2, s2 = fp8_blocks(randn((d, H), std, device, seed, f"{name}.w2", e))
+    return torch.stack([q1, q3]), torch.stack([s1, s3]), q2, s2
+
+
 def gen_experts(n_experts: int, d: int, H: int, seed: int = 0, device="cpu",
-                std: float = 0.02, name: str = "expert") -> ExpertWeights:
-    """n_experts SwiGLU experts with weights ~ N(0, std) stored as block-scaled e4m3."""
-    w13 = torch.empty((n_experts, 2, H, d), dtype=torch.uint8, device=device)
-    w13_s = torch.empty((n_experts, 2, H // BLOCK, d // BLOCK), dtype=torch.float32, device=device)
-    w2 = torch.empty((n_experts, d, H), dtype=torch.uint8, device=device)
-    w2_s = torch.empty((n_experts, d // BLOCK, H // BLOCK), dtype=torch.float32, device=device)
-    for e in range(n_experts):
-        for j, nm in enumerate(("w1", "w3")):
-            q, s = fp8_blocks(randn((H, d), std, device, seed, f"{name}.{nm}", e))
-            w13[e, j].copy_(q)
-            w13_s[e, j].copy_(s)
-        q, s = fp8_blocks(randn((d, H), std, device, seed, f"{name}.w2", e))
-        w2[e].copy_(q)
-        w2_s[e].copy_(s)
+                std: float = 0.02, name: str = "expert", only=None) -> ExpertWeights:
+    """n_experts SwiGLU experts with weights ~ N(0, std) stored as block-scaled e4m3.
+
+    ``only``: generate just these expert ids (the others stay zero)."""
+    w13 = torch.zeros((n_experts, 2, H, d), dtype=torch.uint8, device=device)
+    w13_s = torch.zeros((n_experts, 2, H // BLOCK, d // BLOCK), dtype=torch.float32, device=device)
+    w2 = torch.zeros((n_experts, d, H), dtype=torch.uint8, device=device)
+    w2_s = torch.zeros((n_experts, d // BLOCK, H // BLOCK), dtype=torch.float32, device=device)
+    for e in (range(n_experts) if only is None else sorted(set(only))):
+        a, b, c, f = gen_expert(e, d, H, seed, device, std, name)
+        w13[e].copy_(a)
+        w13_s[e].copy_(b)
+        w2[e].copy_(c)
+        w2_s[e].copy_(f)
     return ExpertWeights(w13, w13_s, w2, w2_s)
 
 

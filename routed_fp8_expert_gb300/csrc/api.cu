@@ -1,0 +1,550 @@
+// C ABI of the routed FP8 MoE FFN forward (declared in include/moe_fp8.h).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "gemm.cuh"
+#include "internal.h"
+#include "moe_fp8.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local char t_err[512] = "no error";
+thread_local int t_launches = 0;
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(call, what)                            \
+    do {                                                \
+        cudaError_t e_ = (call);                        \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+#define MOE_CHECK(expr)             \
+    do {                            \
+        int s_ = (expr);            \
+        if (s_ != MOE_OK) return s_; \
+    } while (0)
+
+constexpr int kMaxT = 1 << 20;
+
+int check_cfg(const moe_cfg_t *c) {
+    if (!c) return fail(MOE_ERR_ARG, "cfg is NULL");
+    if (c->d <= 0 || c->d % 128 || c->d > 16384)
+        return fail(MOE_ERR_UNSUPPORTED, "d=%d must be a multiple of 128 in [128, 16384]", c->d);
+    if (c->H <= 0 || c->H % 128 || c->H > 65536)
+        return fail(MOE_ERR_UNSUPPORTED, "H=%d must be a multiple of 128 in [128, 65536]", c->H);
+    if (c->topk < 1 || c->topk > 32) return fail(MOE_ERR_UNSUPPORTED, "topk=%d must be in [1, 32]", c->topk);
+    if (c->E < c->topk || c->E > 1024)
+        return fail(MOE_ERR_UNSUPPORTED, "E=%d must be in [topk, 1024]", c->E);
+    if (c->n_shared < 0 || c->n_shared > 4) return fail(MOE_ERR_UNSUPPORTED, "n_shared=%d must be in [0, 4]", c->n_shared);
+    if (!std::isfinite(c->route_scale)) return fail(MOE_ERR_ARG, "route_scale is not finite");
+    return MOE_OK;
+}
+
+int check_T(int T) {
+    if (T < 0) return fail(MOE_ERR_ARG, "T=%d is negative", T);
+    if (T > kMaxT) return fail(MOE_ERR_UNSUPPORTED, "T=%d exceeds %d", T, kMaxT);
+    return MOE_OK;
+}
+
+int check_ptr(const void *p, const char *name) {
+    if (!p) return fail(MOE_ERR_ARG, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(p) & 15) return fail(MOE_ERR_ARG, "%s is not 16-byte aligned", name);
+    return MOE_OK;
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// ---------------------------------------------------------------- workspace
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Carver {
+    uint8_t *base;
+    size_t off = 0;
+    template <typename P> P *take(size_t bytes) {
+        off = align_up(off, 1024);
+        P *p = base ? reinterpret_cast<P *>(base + off) : nullptr;
+        off += bytes;
+        return p;
+    }
+};
+
+struct LayerWs {
+    float *logits;
+    uint8_t *xq;
+    float *sx;
+    int32_t *idx;
+    float *w;
+    int32_t *rank, *cnt, *counts, *offsets, *sorted_tok, *inv_pos, *row_start, *tile_prefix;
+    uint8_t *xq_perm;
+    float *sx_perm;
+    uint8_t *hq;
+    float *hs_t;
+    __nv_bfloat16 *o;
+    size_t bytes;
+};
+
+LayerWs carve_layer(const moe_cfg_t &c, int T, void *base) {
+    Carver cv{static_cast<uint8_t *>(base)};
+    const size_t Tz = static_cast<size_t>(T);
+    const size_t R = static_cast<size_t>(c.topk + c.n_shared) * Tz;
+    const size_t C = (Tz + 31) / 32;
+    const size_t G = static_cast<size_t>(c.E + c.n_shared);
+    LayerWs w{};
+    w.logits = cv.take<float>(Tz * c.E * 4);
+    w.xq = cv.take<uint8_t>(Tz * c.d);
+    w.sx = cv.take<float>(Tz * (c.d / 128) * 4);
+    w.idx = cv.take<int32_t>(Tz * c.topk * 4);
+    w.w = cv.take<float>(Tz * c.topk * 4);
+    w.rank = cv.take<int32_t>(Tz * c.topk * 4);
+    w.cnt = cv.take<int32_t>(C * c.E * 4);
+    w.counts = cv.take<int32_t>(static_cast<size_t>(c.E) * 4);
+    w.offsets = cv.take<int32_t>(static_cast<size_t>(c.E + 1) * 4);
+    w.sorted_tok = cv.take<int32_t>(Tz * c.topk * 4);
+    w.inv_pos = cv.take<int32_t>(Tz * c.topk * 4);
+    w.row_start = cv.take<int32_t>((G + 1) * 4);
+    w.tile_prefix = cv.take<int32_t>((G + 1) * 4);
+    w.xq_perm = cv.take<uint8_t>(R * c.d);
+    w.sx_perm = cv.take<float>(R * (c.d / 128) * 4);
+    w.hq = cv.take<uint8_t>(R * c.H);
+    w.hs_t = cv.take<float>(R * (c.H / 128) * 4);
+    w.o = cv.take<__nv_bfloat16>(R * c.d * 2);
+    w.bytes = align_up(cv.off, 1024);
+    return w;
+}
+
+int check_ws(const void *ws, size_t have, size_t need) {
+    if (have < need) return fail(MOE_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed", have, need);
+    return check_ptr(ws, "workspace");
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D row-major matrix [rows, cols] of 1- or 2-byte elements; box = 128 bytes x box_rows,
+// 128-byte swizzle (the canonical K-major layout of the MMA operands).
+int make_map(CUtensorMap *m, const void *ptr, int elem_bytes, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * elem_bytes};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- steps
+
+int route_impl(const void *x, const void *wg, const float *bias, const moe_cfg_t &c, int T, int32_t *idx,
+               float *w, float *scores, float *logits, cudaStream_t st) {
+    CUtensorMap ma, mb;
+    MOE_CHECK(make_map(&ma, wg, 2, c.E, c.d, kBM));
+    MOE_CHECK(make_map(&mb, x, 2, T, c.d, kActBoxRows));
+    GemmArgs a{};
+    a.G = 1;
+    a.num_kb = c.d / 64;
+    a.num_mb = (c.E + kBM - 1) / kBM;
+    a.total_rows = T;
+    a.single_rows = T;
+    a.logits = logits;
+    a.n_valid = c.E;
+    const int items = a.num_mb * ((T + kBN - 1) / kBN);
+    MOE_CUDA(launch_grouped_gemm(Kind::Router, ma, mb, a, std::min(items, num_sms()), st), "router GEMM launch");
+    MOE_CUDA(launch_topk(logits, bias, T, c.E, c.topk, c.route_scale, idx, w, scores, st), "top-k launch");
+    t_launches += 2;
+    return MOE_OK;
+}
+
+int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets, const uint8_t *w13,
+                const float *w13_s, const moe_cfg_t &c, int T, uint8_t *hq, float *hs, const LayerWs &ws,
+                bool run_sched, cudaStream_t st) {
+    const int G = c.E + c.n_shared;
+    const int64_t R = static_cast<int64_t>(c.topk + c.n_shared) * T;
+    if (run_sched) {
+        MOE_CUDA(launch_sched(offsets, c.E, c.n_shared, T, c.topk, kBN, ws.row_start, ws.tile_prefix, st),
+                 "schedule launch");
+        t_launches += 1;
+    }
+    CUtensorMap m13, mx;
+    MOE_CHECK(make_map(&m13, w13, 1, static_cast<uint64_t>(G) * 2 * c.H, c.d, kBM));
+    MOE_CHECK(make_map(&mx, xq_perm, 1, R, c.d, kActBoxRows));
+    GemmArgs gu{};
+    gu.G = G;
+    gu.num_kb = c.d / 128;
+    gu.num_mb = c.H / 128;
+    gu.total_rows = static_cast<int>(R);
+    gu.single_rows = -1;
+    gu.row_start = ws.row_start;
+    gu.tile_prefix = ws.tile_prefix;
+    gu.act_scale_t = sx_perm;
+    gu.w_scale = w13_s;
+    gu.a_rows_per_group = 2 * c.H;
+    gu.a_second_offset = c.H;
+    gu.hq = hq;
+    gu.hs_t = hs;
+    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
+    t_launches += 1;
+    return MOE_OK;
+}
+
+int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const uint8_t *w2, const float *w2_s,
+              const moe_cfg_t &c, int T, void *o, const LayerWs &ws, bool run_sched, cudaStream_t st) {
+    const int G = c.E + c.n_shared;
+    const int64_t R = static_cast<int64_t>(c.topk + c.n_shared) * T;
+    if (run_sched) {
+        MOE_CUDA(launch_sched(offsets, c.E, c.n_shared, T, c.topk, kBN, ws.row_start, ws.tile_prefix, st),
+                 "schedule launch");
+        t_launches += 1;
+    }
+    CUtensorMap m2, mh;
+    MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, kBM));
+    MOE_CHECK(make_map(&mh, hq, 1, R, c.H, kActBoxRows));
+    GemmArgs dn{};
+    dn.G = G;
+    dn.num_kb = c.H / 128;
+    dn.num_mb = c.d / 128;
+    dn.total_rows = static_cast<int>(R);
+    dn.single_rows = -1;
+    dn.row_start = ws.row_start;
+    dn.tile_prefix = ws.tile_prefix;
+    dn.act_scale_t = hs;
+    dn.w_scale = w2_s;
+    dn.a_rows_per_group = c.d;
+    dn.out = static_cast<__nv_bfloat16 *>(o);
+    MOE_CUDA(launch_grouped_gemm(Kind::Down, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    t_launches += 1;
+    return MOE_OK;
+}
+
+int experts_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets, const uint8_t *w13,
+                 const float *w13_s, const uint8_t *w2, const float *w2_s, const moe_cfg_t &c, int T, void *o,
+                 const LayerWs &ws, cudaStream_t st) {
+    MOE_CHECK(gateup_impl(xq_perm, sx_perm, offsets, w13, w13_s, c, T, ws.hq, ws.hs_t, ws, true, st));
+    return down_impl(ws.hq, ws.hs_t, offsets, w2, w2_s, c, T, o, ws, false, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_permuted_rows(const moe_cfg_t *cfg, int T) {
+    if (!cfg || T < 0) return 0;
+    return static_cast<int64_t>(cfg->topk + cfg->n_shared) * T;
+}
+
+size_t moe_workspace_bytes(const moe_cfg_t *cfg, int T) {
+    if (check_cfg(cfg) != MOE_OK || check_T(T) != MOE_OK) return 0;
+    return carve_layer(*cfg, T, nullptr).bytes;
+}
+
+int moe_quant_fp8_1x128(const void *in, int in_is_bf16, int64_t rows, int cols, uint8_t *q, float *s,
+                        int s_transposed, void *stream) {
+    t_launches = 0;
+    if (rows < 0) return fail(MOE_ERR_ARG, "rows=%lld is negative", static_cast<long long>(rows));
+    if (cols <= 0 || cols % 128) return fail(MOE_ERR_UNSUPPORTED, "cols=%d must be a positive multiple of 128", cols);
+    if (rows == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(in, "in"));
+    MOE_CHECK(check_ptr(q, "q"));
+    if (!s) return fail(MOE_ERR_ARG, "s is NULL");
+    MOE_CUDA(launch_quant(in, in_is_bf16 != 0, rows, cols, q, s, s_transposed != 0, num_sms(),
+                          static_cast<cudaStream_t>(stream)),
+             "quantise launch");
+    t_launches = 1;
+    return MOE_OK;
+}
+
+int moe_route(const void *x, const void *w_gate, const float *bias, const moe_cfg_t *cfg, int T, int32_t *topk_idx,
+              float *topk_w, float *scores, void *workspace, size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(x, "x"));
+    MOE_CHECK(check_ptr(w_gate, "w_gate"));
+    if (!bias) return fail(MOE_ERR_ARG, "bias is NULL");
+    MOE_CHECK(check_ptr(topk_idx, "topk_idx"));
+    MOE_CHECK(check_ptr(topk_w, "topk_w"));
+    const LayerWs need = carve_layer(*cfg, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(*cfg, T, workspace);
+    return route_impl(x, w_gate, bias, *cfg, T, topk_idx, topk_w, scores, ws.logits, static_cast<cudaStream_t>(stream));
+}
+
+int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx, const moe_cfg_t *cfg, int T,
+                int32_t *offsets, int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm, float *sx_perm,
+                void *workspace, size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(topk_idx, "topk_idx"));
+    MOE_CHECK(check_ptr(xq, "xq"));
+    MOE_CHECK(check_ptr(sx, "sx"));
+    MOE_CHECK(check_ptr(offsets, "offsets"));
+    MOE_CHECK(check_ptr(sorted_tok, "sorted_tok"));
+    MOE_CHECK(check_ptr(inv_pos, "inv_pos"));
+    MOE_CHECK(check_ptr(xq_perm, "xq_perm"));
+    MOE_CHECK(check_ptr(sx_perm, "sx_perm"));
+    const LayerWs need = carve_layer(*cfg, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(*cfg, T, workspace);
+    int n = 0;
+    MOE_CUDA(launch_permute(topk_idx, xq, sx, T, cfg->topk, cfg->n_shared, cfg->E, cfg->d, ws.rank, ws.cnt,
+                            ws.counts, offsets, sorted_tok, inv_pos, xq_perm, sx_perm, &n,
+                            static_cast<cudaStream_t>(stream)),
+             "permutation launch");
+    t_launches = n;
+    return MOE_OK;
+}
+
+int moe_expert_gemm_fp8(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets, const uint8_t *w13,
+                        const float *w13_s, const uint8_t *w2, const float *w2_s, const moe_cfg_t *cfg, int T,
+                        void *o, void *workspace, size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(xq_perm, "xq_perm"));
+    MOE_CHECK(check_ptr(sx_perm, "sx_perm"));
+    MOE_CHECK(check_ptr(offsets, "offsets"));
+    MOE_CHECK(check_ptr(w13, "w13"));
+    MOE_CHECK(check_ptr(w13_s, "w13_s"));
+    MOE_CHECK(check_ptr(w2, "w2"));
+    MOE_CHECK(check_ptr(w2_s, "w2_s"));
+    MOE_CHECK(check_ptr(o, "o"));
+    const LayerWs need = carve_layer(*cfg, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(*cfg, T, workspace);
+    return experts_impl(xq_perm, sx_perm, offsets, w13, w13_s, w2, w2_s, *cfg, T, o, ws,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_gateup_fp8(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets,
+                          const uint8_t *w13, const float *w13_s, const moe_cfg_t *cfg, int T, uint8_t *hq,
+                          float *hs, void *workspace, size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(xq_perm, "xq_perm"));
+    MOE_CHECK(check_ptr(sx_perm, "sx_perm"));
+    MOE_CHECK(check_ptr(offsets, "offsets"));
+    MOE_CHECK(check_ptr(w13, "w13"));
+    MOE_CHECK(check_ptr(w13_s, "w13_s"));
+    MOE_CHECK(check_ptr(hq, "hq"));
+    MOE_CHECK(check_ptr(hs, "hs"));
+    const LayerWs need = carve_layer(*cfg, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(*cfg, T, workspace);
+    return gateup_impl(xq_perm, sx_perm, offsets, w13, w13_s, *cfg, T, hq, hs, ws, true,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_down_fp8(const uint8_t *hq, const float *hs, const int32_t *offsets, const uint8_t *w2,
+                        const float *w2_s, const moe_cfg_t *cfg, int T, void *o, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(hq, "hq"));
+    MOE_CHECK(check_ptr(hs, "hs"));
+    MOE_CHECK(check_ptr(offsets, "offsets"));
+    MOE_CHECK(check_ptr(w2, "w2"));
+    MOE_CHECK(check_ptr(w2_s, "w2_s"));
+    MOE_CHECK(check_ptr(o, "o"));
+    const LayerWs need = carve_layer(*cfg, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(*cfg, T, workspace);
+    return down_impl(hq, hs, offsets, w2, w2_s, *cfg, T, o, ws, true, static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const void *o, const float *topk_w, const int32_t *inv_pos, const moe_cfg_t *cfg, int T, void *y,
+                void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(o, "o"));
+    MOE_CHECK(check_ptr(topk_w, "topk_w"));
+    MOE_CHECK(check_ptr(inv_pos, "inv_pos"));
+    MOE_CHECK(check_ptr(y, "y"));
+    MOE_CUDA(launch_combine(o, topk_w, inv_pos, T, cfg->topk, cfg->n_shared, cfg->d, y,
+                            static_cast<cudaStream_t>(stream)),
+             "combine launch");
+    t_launches = 1;
+    return MOE_OK;
+}
+
+int moe_layer_forward(const void *x, const void *w_gate, const float *bias, const uint8_t *w13, const float *w13_s,
+                      const uint8_t *w2, const float *w2_s, const moe_cfg_t *cfg, int T, void *y, int32_t *topk_idx,
+                      float *topk_w, void *workspace, size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(x, "x"));
+    MOE_CHECK(check_ptr(w_gate, "w_gate"));
+    if (!bias) return fail(MOE_ERR_ARG, "bias is NULL");
+    MOE_CHECK(check_ptr(w13, "w13"));
+    MOE_CHECK(check_ptr(w13_s, "w13_s"));
+    MOE_CHECK(check_ptr(w2, "w2"));
+    MOE_CHECK(check_ptr(w2_s, "w2_s"));
+    MOE_CHECK(check_ptr(y, "y"));
+    if (topk_idx) MOE_CHECK(check_ptr(topk_idx, "topk_idx"));
+    if (topk_w) MOE_CHECK(check_ptr(topk_w, "topk_w"));
+    const moe_cfg_t &c = *cfg;
+    const LayerWs need = carve_layer(c, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(c, T, workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t *idx = topk_idx ? topk_idx : ws.idx;
+    float *w = topk_w ? topk_w : ws.w;
+    int n = 0;
+    MOE_CHECK(route_impl(x, w_gate, bias, c, T, idx, w, nullptr, ws.logits, st));
+    n += t_launches;
+    MOE_CUDA(launch_quant(x, true, T, c.d, ws.xq, ws.sx, false, num_sms(), st), "quantise launch");
+    n += 1;
+    int np = 0;
+    MOE_CUDA(launch_permute(idx, ws.xq, ws.sx, T, c.topk, c.n_shared, c.E, c.d, ws.rank, ws.cnt, ws.counts,
+                            ws.offsets, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st),
+             "permutation launch");
+    n += np;
+    t_launches = 0;
+    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, st));
+    n += t_launches;
+    MOE_CUDA(launch_combine(ws.o, w, ws.inv_pos, T, c.topk, c.n_shared, c.d, y, st), "combine launch");
+    n += 1;
+    t_launches = n;
+    return MOE_OK;
+}
+
+size_t dense_swiglu_workspace_bytes(int d, int H, int T) {
+    if (d <= 0 || d % 128 || H <= 0 || H % 128 || T < 0 || T > kMaxT) return 0;
+    Carver cv{nullptr};
+    const size_t Tz = static_cast<size_t>(T);
+    cv.take<uint8_t>(Tz * d);
+    cv.take<float>(Tz * (d / 128) * 4);
+    cv.take<uint8_t>(Tz * H);
+    cv.take<float>(Tz * (H / 128) * 4);
+    return align_up(cv.off, 1024);
+}
+
+int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, const uint8_t *w2, const float *w2_s,
+                     int d, int H, int T, void *y, void *workspace, size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    if (d <= 0 || d % 128 || d > 65536) return fail(MOE_ERR_UNSUPPORTED, "d=%d must be a multiple of 128", d);
+    if (H <= 0 || H % 128 || H > 65536) return fail(MOE_ERR_UNSUPPORTED, "H=%d must be a multiple of 128", H);
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(x, "x"));
+    MOE_CHECK(check_ptr(w13, "w13"));
+    MOE_CHECK(check_ptr(w13_s, "w13_s"));
+    MOE_CHECK(check_ptr(w2, "w2"));
+    MOE_CHECK(check_ptr(w2_s, "w2_s"));
+    MOE_CHECK(check_ptr(y, "y"));
+    MOE_CHECK(check_ws(workspace, workspace_bytes, dense_swiglu_workspace_bytes(d, H, T)));
+    Carver cv{static_cast<uint8_t *>(workspace)};
+    const size_t Tz = static_cast<size_t>(T);
+    uint8_t *xq = cv.take<uint8_t>(Tz * d);
+    float *sx_t = cv.take<float>(Tz * (d / 128) * 4);
+    uint8_t *hq = cv.take<uint8_t>(Tz * H);
+    float *hs_t = cv.take<float>(Tz * (H / 128) * 4);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    MOE_CUDA(launch_quant(x, true, T, d, xq, sx_t, true, num_sms(), st), "quantise launch");
+    CUtensorMap m13, mx, m2, mh;
+    MOE_CHECK(make_map(&m13, w13, 1, static_cast<uint64_t>(2) * H, d, kBM));
+    MOE_CHECK(make_map(&mx, xq, 1, T, d, kActBoxRows));
+    MOE_CHECK(make_map(&m2, w2, 1, d, H, kBM));
+    MOE_CHECK(make_map(&mh, hq, 1, T, H, kActBoxRows));
+    GemmArgs gu{};
+    gu.G = 1;
+    gu.num_kb = d / 128;
+    gu.num_mb = H / 128;
+    gu.total_rows = T;
+    gu.single_rows = T;
+    gu.act_scale_t = sx_t;
+    gu.w_scale = w13_s;
+    gu.a_rows_per_group = 2 * H;
+    gu.a_second_offset = H;
+    gu.hq = hq;
+    gu.hs_t = hs_t;
+    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
+    GemmArgs dn{};
+    dn.G = 1;
+    dn.num_kb = H / 128;
+    dn.num_mb = d / 128;
+    dn.total_rows = T;
+    dn.single_rows = T;
+    dn.act_scale_t = hs_t;
+    dn.w_scale = w2_s;
+    dn.a_rows_per_group = d;
+    dn.out = static_cast<__nv_bfloat16 *>(y);
+    MOE_CUDA(launch_grouped_gemm(Kind::Down, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    t_launches = 3;
+    return MOE_OK;
+}
+
+int moe_check_device_error(void *stream, uint32_t *detail) {
+    unsigned int *word = nullptr;
+    MOE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronise");
+    MOE_CUDA(device_error_word(&word), "error word address");
+    unsigned int v = 0;
+    MOE_CUDA(cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost), "error word read");
+    if (v) MOE_CUDA(cudaMemset(word, 0, sizeof(v)), "error word clear");
+    if (detail) *detail = v;
+    if (v) return fail(MOE_ERR_TIMEOUT, "device error bits 0x%x (a bounded wait gave up)", v);
+    return MOE_OK;
+}
+
+const char *moe_last_error_string(void) { return t_err; }
+
+int moe_last_launch_count(void) { return t_launches; }
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Launchers of the quantise / top-k / permutation / combine kernels.
+#include "kernels.cuh"
+#include "internal.h"
+#include "gemm.cuh"
+
+namespace moe {
+
+cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint8_t *q, float *s,
+                         bool s_transposed, int num_sms, cudaStream_t stream) {
+    const int64_t groups = rows * (cols / 128);
+    const int threads = 256;
+    int64_t blocks = (groups + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    if (bf16)
+        quant_1x128_kernel<true><<<static_cast<int>(blocks), threads, 0, stream>>>(in, rows, cols, q, s, s_transposed);
+    else
+        quant_1x128_kernel<false><<<static_cast<int>(blocks), threads, 0, stream>>>(in, rows, cols, q, s, s_transposed);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float *logits, const float *bias, int T, int E, int k, float scale,
+                        int32_t *idx, float *w, float *scores, cudaStream_t stream) {
+    const int threads = 256;  // 8 tokens per block
+    topk_kernel<<<(T + 7) / 8, threads, 0, stream>>>(logits, bias, T, E, k, scale, idx, w, scores);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *sx, int T, int k, int S, int E,
+                           int d, int32_t *rank, int32_t *cnt, int32_t *counts, int32_t *offsets,
+                           int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm, float *sx_perm,
+                           int *launches, cudaStream_t stream) {
+    const int C = (T + 31) / 32;
+    cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * static_cast<size_t>(E) * C, stream);
+    if (e != cudaSuccess) return e;
+    const size_t smem = sizeof(int32_t) * kPermWarps * 32 * k;
+    perm_rank_kernel<<<(C + kPermWarps - 1) / kPermWarps, kPermWarps * 32, smem, stream>>>(idx, T, k, C, rank, cnt);
+    perm_scan_kernel<<<E, 256, 0, stream>>>(cnt, C, counts);
+    perm_offsets_kernel<<<1, 1024, 0, stream>>>(counts, E, offsets);
+    const int threads = min(1024, max(64, d / 16));
+    perm_scatter_kernel<<<T, threads, 0, stream>>>(idx, rank, cnt, offsets, xq, sx, T, k, S, d, C, sorted_tok,
+                                                   inv_pos, xq_perm, sx_perm);
+    *launches += 4;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile, int32_t *row_start,
+                         int32_t *tile_prefix, cudaStream_t stream) {
+    sched_kernel<<<1, 1024, 0, stream>>>(offsets, E, S, T, k, tile, row_start, tile_prefix);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos, int T, int k, int S, int d,
+                           void *y, cudaStream_t stream) {
+    const int threads = min(256, max(32, d / 8));
+    combine_kernel<<<T, threads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d,
+                                              static_cast<__nv_bfloat16 *>(y));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

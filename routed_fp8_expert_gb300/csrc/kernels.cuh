@@ -1,0 +1,342 @@
+// Bandwidth- and latency-bound kernels of the MoE layer: 1x128 activation
+// quantisation, router top-k, token permutation and the weighted combine.
+#pragma once
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ------------------------------------------------------------------ quantise
+// One warp per 128-wide group: lane l holds elements 4l..4l+3.
+// s = amax / 448 (IEEE fp32 division), q = e4m3(x / s) (IEEE division, RNE,
+// saturating); amax = 0 gives s = 0 and zero codes.
+template <bool kBf16In>
+__global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, int cols,
+                                   uint8_t *__restrict__ q, float *__restrict__ s, int s_transposed) {
+    const int lane = threadIdx.x & 31;
+    const int gpr = cols / 128;
+    const int64_t n_groups = rows * gpr;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t gi = warp0; gi < n_groups; gi += nwarps) {
+        const int64_t r = gi / gpr;
+        const int g = static_cast<int>(gi - r * gpr);
+        const int64_t base = r * cols + g * 128 + lane * 4;
+        float v[4];
+        if constexpr (kBf16In) {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(in) + base);
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+            v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
+        } else {
+            const float4 f = *reinterpret_cast<const float4 *>(static_cast<const float *>(in) + base);
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        }
+        unsigned m = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = max(m, __float_as_uint(fabsf(v[i])));
+        const float amax = __uint_as_float(__reduce_max_sync(kFull, m));
+        const float sc = amax / 448.0f;
+        uint32_t packed = 0;
+        if (amax != 0.f) {
+            const uint32_t lo = e4m3x2(v[0] / sc, v[1] / sc);
+            const uint32_t hi = e4m3x2(v[2] / sc, v[3] / sc);
+            packed = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint32_t *>(q + base) = packed;
+        if (lane == 0) s[s_transposed ? (static_cast<int64_t>(g) * rows + r) : (r * gpr + g)] = sc;
+    }
+}
+
+// ------------------------------------------------------------------ top-k
+// One warp per token. Scores s = sigmoid(logit) in fp32; choice c = s + bias;
+// k rounds of a warp arg-max on (c desc, expert id asc); weights from s.
+__global__ void topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E,
+                            int k, float route_scale, int32_t *__restrict__ topk_idx,
+                            float *__restrict__ topk_w, float *__restrict__ scores) {
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const float *lrow = logits + static_cast<size_t>(t) * E;
+    float sv[32], cv[32];
+    const int nper = (E + 31) >> 5;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        if (i < nper && e < E) {
+            const float sc = 1.0f / (1.0f + expf(-lrow[e]));
+            sv[i] = sc;
+            cv[i] = sc + bias[e];
+            if (scores) scores[static_cast<size_t>(t) * E + e] = sc;
+        } else {
+            sv[i] = 0.f;
+            cv[i] = -INFINITY;
+        }
+    }
+    int my_idx = 0;
+    float my_s = 0.f;
+    for (int r = 0; r < k; ++r) {
+        float best = -INFINITY;
+        int best_e = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (i < nper && cv[i] > best) { best = cv[i]; best_e = lane + 32 * i; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ob = __shfl_xor_sync(kFull, best, off);
+            const int oe = __shfl_xor_sync(kFull, best_e, off);
+            if (ob > best || (ob == best && oe < best_e)) { best = ob; best_e = oe; }
+        }
+        const int owner = best_e & 31;
+        const int slot = best_e >> 5;
+        float mine = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (i == slot && lane == owner) { mine = sv[i]; cv[i] = -INFINITY; }
+        }
+        const float s_sel = __shfl_sync(kFull, mine, owner);
+        if (lane == r) { my_idx = best_e; my_s = s_sel; }
+    }
+    float sum = (lane < k) ? my_s : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < k) {
+        topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
+        topk_w[static_cast<size_t>(t) * k + lane] = my_s / sum * route_scale;
+    }
+}
+
+// ------------------------------------------------------------------ permutation
+// Tokens are processed in chunks of 32 (one warp). For assignment (t, j) to
+// expert e:
+//   rank[t, j]   = number of tokens t' < t in t's chunk that also chose e
+//   cnt[e][c]    = number of tokens of chunk c that chose e
+// then cnt is scanned over chunks (per expert) and over experts, giving
+//   position(t, j) = offsets[e] + sum_{c' < c} cnt[e][c'] + rank[t, j],
+// the ascending-token order inside every expert segment.
+constexpr int kPermWarps = 8;
+
+__global__ void perm_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int C,
+                                 int32_t *__restrict__ rank, int32_t *__restrict__ cnt) {
+    extern __shared__ int32_t s_ids[];  // [kPermWarps][32 * k]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * kPermWarps + warp;
+    if (c >= C) return;
+    int32_t *ids = s_ids + warp * 32 * k;
+    const int t = c * 32 + lane;
+    for (int j = 0; j < k; ++j) ids[lane * k + j] = (t < T) ? idx[static_cast<size_t>(t) * k + j] : -1;
+    __syncwarp();
+    if (t >= T) return;
+    for (int j = 0; j < k; ++j) {
+        const int e = ids[lane * k + j];
+        int before = 0, after = 0;
+        for (int l = 0; l < 32; ++l) {
+            if (l == lane) continue;
+            for (int jj = 0; jj < k; ++jj) {
+                if (ids[l * k + jj] == e) {
+                    if (l < lane) ++before; else ++after;
+                }
+            }
+        }
+        rank[static_cast<size_t>(t) * k + j] = before;
+        if (after == 0) cnt[static_cast<size_t>(e) * C + c] = before + 1;
+    }
+}
+
+// Exclusive scan of one expert's per-chunk counts (in place); total -> counts[e].
+__global__ void perm_scan_kernel(int32_t *__restrict__ cnt, int C, int32_t *__restrict__ counts) {
+    __shared__ int32_t s_warp[32];
+    __shared__ int32_t s_carry;
+    const int e = blockIdx.x;
+    int32_t *row = cnt + static_cast<size_t>(e) * C;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < C; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const int v = (i < C) ? row[i] : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = (lane < nw) ? s_warp[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, w, off);
+                if (lane >= off) w += o;
+            }
+            s_warp[lane] = w;  // inclusive scan of warp totals
+        }
+        __syncthreads();
+        const int carry = s_carry;
+        const int excl = carry + (warp > 0 ? s_warp[warp - 1] : 0) + incl - v;
+        if (i < C) row[i] = excl;
+        __syncthreads();
+        if (threadIdx.x == 0) s_carry = carry + s_warp[nw - 1];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) counts[e] = s_carry;
+}
+
+// Block-wide exclusive scan of up to blockDim.x * kItems values (single block).
+template <int kItems>
+__device__ void block_exclusive_scan(const int32_t *in, int n, int32_t *out, int32_t *total) {
+    __shared__ int32_t s_warp[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int v[kItems];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        const int idx = threadIdx.x * kItems + i;
+        v[i] = (idx < n) ? in[idx] : 0;
+        local += v[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < nw) ? s_warp[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, w, off);
+            if (lane >= off) w += o;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    int run = (warp > 0 ? s_warp[warp - 1] : 0) + incl - local;
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        const int idx = threadIdx.x * kItems + i;
+        if (idx < n) out[idx] = run;
+        run += v[i];
+    }
+    if (total && threadIdx.x == 0) *total = s_warp[nw - 1];
+    __syncthreads();
+}
+
+// offsets[0..E] from counts[0..E-1]. Single block of 1024 threads (E <= 1024).
+__global__ void perm_offsets_kernel(const int32_t *__restrict__ counts, int E, int32_t *__restrict__ offsets) {
+    block_exclusive_scan<1>(counts, E, offsets, offsets + E);
+}
+
+// Segment table of the grouped GEMM: groups 0..E-1 are the routed experts'
+// segments (offsets), groups E..E+S-1 the shared experts' T rows each.
+//   row_start[g]   first activation row of group g; row_start[E+S] = (k+S)*T
+//   tile_prefix[g] prefix sum of ceil(rows_g / tile) over groups
+// Single block of 1024 threads (E + S <= 1028).
+__global__ void sched_kernel(const int32_t *__restrict__ offsets, int E, int S, int T, int k, int tile,
+                             int32_t *__restrict__ row_start, int32_t *__restrict__ tile_prefix) {
+    __shared__ int32_t s_tiles[2048];
+    const int G = E + S;
+    const int kT = k * T;
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+        const int rs = (g <= E) ? offsets[g] : kT + (g - E) * T;
+        row_start[g] = rs;
+    }
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const int a = (g < E) ? offsets[g] : kT + (g - E) * T;
+        const int b = (g < E) ? offsets[g + 1] : kT + (g - E + 1) * T;
+        s_tiles[g] = (b - a + tile - 1) / tile;
+    }
+    __syncthreads();
+    block_exclusive_scan<2>(s_tiles, G, tile_prefix, tile_prefix + G);
+}
+
+// One block per token: writes sorted_tok / inv_pos and copies the token's
+// quantised row and scales to its k routed positions and its S shared rows.
+// sx is row-major [T, d/128]; sx_perm is K-block-major [d/128, R].
+__global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ rank,
+                                    const int32_t *__restrict__ cnt_scan, const int32_t *__restrict__ offsets,
+                                    const uint8_t *__restrict__ xq, const float *__restrict__ sx, int T, int k,
+                                    int S, int d, int C, int32_t *__restrict__ sorted_tok,
+                                    int32_t *__restrict__ inv_pos, uint8_t *__restrict__ xq_perm,
+                                    float *__restrict__ sx_perm) {
+    __shared__ int32_t s_pos[40];
+    const int t = blockIdx.x;
+    const int c = t >> 5;
+    const int64_t R = static_cast<int64_t>(k + S) * T;
+    const int ndst = k + S;
+    if (threadIdx.x < k) {
+        const int j = threadIdx.x;
+        const int e = idx[static_cast<size_t>(t) * k + j];
+        const int pos = offsets[e] + cnt_scan[static_cast<size_t>(e) * C + c] + rank[static_cast<size_t>(t) * k + j];
+        s_pos[j] = pos;
+        inv_pos[static_cast<size_t>(t) * k + j] = pos;
+        sorted_tok[pos] = t;
+    } else if (threadIdx.x < ndst) {
+        s_pos[threadIdx.x] = k * T + (threadIdx.x - k) * T + t;
+    }
+    __syncthreads();
+    const uint4 *src = reinterpret_cast<const uint4 *>(xq + static_cast<size_t>(t) * d);
+    const int nvec = d / 16;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+        const uint4 val = src[v];
+        for (int j = 0; j < ndst; ++j)
+            reinterpret_cast<uint4 *>(xq_perm + static_cast<size_t>(s_pos[j]) * d)[v] = val;
+    }
+    const int gpr = d / 128;
+    for (int g = threadIdx.x; g < gpr; g += blockDim.x) {
+        const float sc = sx[static_cast<size_t>(t) * gpr + g];
+        for (int j = 0; j < ndst; ++j) sx_perm[static_cast<size_t>(g) * R + s_pos[j]] = sc;
+    }
+}
+
+// ------------------------------------------------------------------ combine
+// y[t] = sum_s o[kT + sT + t] + sum_j w[t, j] * o[inv_pos[t, j]] (fp32, fixed order) -> bf16.
+__global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w,
+                               const int32_t *__restrict__ inv_pos, int T, int k, int S, int d,
+                               __nv_bfloat16 *__restrict__ y) {
+    __shared__ int32_t s_pos[32];
+    __shared__ float s_w[32];
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) {
+        s_pos[threadIdx.x] = inv_pos[static_cast<size_t>(t) * k + threadIdx.x];
+        s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
+    }
+    __syncthreads();
+    const int nvec = d / 8;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int s = 0; s < S; ++s) {
+            const uint4 raw = reinterpret_cast<const uint4 *>(o + (static_cast<size_t>(k) * T + static_cast<size_t>(s) * T + t) * d)[v];
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += __low2float(h[i]);
+                acc[2 * i + 1] += __high2float(h[i]);
+            }
+        }
+        for (int j = 0; j < k; ++j) {
+            const uint4 raw = reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v];
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+            const float wj = s_w[j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj, __low2float(h[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, __high2float(h[i]), acc[2 * i + 1]);
+            }
+        }
+        uint4 out;
+        __nv_bfloat162 *oh = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) oh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * d)[v] = out;
+    }
+}
+
+}  // namespace moe
