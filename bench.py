@@ -45,8 +45,11 @@ METRIC = "MoE-layer tokens/s (d7168, 384e top-8, FP8) + % of HBM / FP8-TC roofli
 # decode_e64: the decode layer with 64 routed experts and 48 tokens (about 6 rows per
 # expert, as at T=256 with 384 experts; 2.9 GB of weights): a profiling case of a few GB
 DECODE_E64 = S.MoEShape("kimi_k2_moe_decode_e64_t48", T=48, d=7168, E=64, topk=8, H=2048)
+# prefill_e64: 64 routed experts and 768 tokens (96 rows per expert, the 128-token
+# tile path of the prefill batch; 2.9 GB of weights)
+PREFILL_E64 = S.MoEShape("kimi_k2_moe_prefill_e64_t768", T=768, d=7168, E=64, topk=8, H=2048)
 WORKLOADS = {"decode": S.DECODE, "prefill": S.PREFILL, "skewed": S.SKEWED, "dense": S.DENSE, "toy": S.TOY,
-             "decode_e64": DECODE_E64}
+             "decode_e64": DECODE_E64, "prefill_e64": PREFILL_E64}
 DATA = ("synthetic, seeded: x ~ N(0,1) bf16; W_g ~ N(0,0.02) bf16; bias ~ N(0,0.01) fp32 (+0.5 on 16 hot "
         "experts for the skewed workload); expert weights ~ N(0,0.02) stored e4m3 with 128x128 fp32 scales")
 

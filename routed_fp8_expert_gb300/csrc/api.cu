@@ -1,6 +1,7 @@
 // C ABI of the routed FP8 MoE FFN forward (declared in include/moe_fp8.h).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -82,6 +83,36 @@ int num_sms() {
     return cache[dev];
 }
 
+// Token-tile width of the expert GEMMs: expected rows per routed expert k*T/E
+// decides. Narrow tiles leave more shared memory to the weight pipeline; the
+// 64-token tile keeps every TMEM chunk of a K block in registers at once.
+int expert_bn(const moe_cfg_t &c, int T) {
+    const double rows = static_cast<double>(c.topk) * T / c.E;
+    return rows <= 12.0 ? 32 : 64;
+}
+
+// The down GEMM's epilogue holds one accumulator per column, so it can take
+// 128-token tiles beyond the decode regime (half the items and weight passes).
+int down_bn(const moe_cfg_t &c, int T) {
+    const double rows = static_cast<double>(c.topk) * T / c.E;
+    if (rows <= 12.0) return 32;
+    return rows <= 40.0 ? 64 : 128;
+}
+
+int router_bn(int T) { return T <= 512 ? 32 : 128; }
+
+// Deterministic split-K of the router GEMM so that small batches still cover
+// the GPU in one wave: at most 148 work items, at least 4 K blocks (of 64
+// elements) per split.
+int router_splits(const moe_cfg_t &c, int T) {
+    const int bn = router_bn(T);
+    const int items = std::max(1, ((T + bn - 1) / bn) * ((c.E + 127) / 128));
+    int s = 148 / items;
+    const int max_by_k = std::max(1, (c.d / 64) / 4);
+    s = std::min(s, std::min(8, max_by_k));
+    return std::max(1, s);
+}
+
 // ---------------------------------------------------------------- workspace
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -103,7 +134,8 @@ struct LayerWs {
     float *sx;
     int32_t *idx;
     float *w;
-    int32_t *rank, *cnt, *counts, *offsets, *sorted_tok, *inv_pos, *row_start, *tile_prefix;
+    int32_t *rank, *cnt, *counts, *offsets, *sorted_tok, *inv_pos, *row_start, *tile_prefix, *tile_prefix_dn;
+    int32_t *counters;  // [2] dynamic scheduler counters of the gate/up and down GEMMs
     uint8_t *xq_perm;
     float *sx_perm;
     uint8_t *hq;
@@ -119,19 +151,21 @@ LayerWs carve_layer(const moe_cfg_t &c, int T, void *base) {
     const size_t C = (Tz + 31) / 32;
     const size_t G = static_cast<size_t>(c.E + c.n_shared);
     LayerWs w{};
-    w.logits = cv.take<float>(Tz * c.E * 4);
+    w.logits = cv.take<float>(static_cast<size_t>(router_splits(c, T)) * Tz * c.E * 4);
     w.xq = cv.take<uint8_t>(Tz * c.d);
     w.sx = cv.take<float>(Tz * (c.d / 128) * 4);
     w.idx = cv.take<int32_t>(Tz * c.topk * 4);
     w.w = cv.take<float>(Tz * c.topk * 4);
     w.rank = cv.take<int32_t>(Tz * c.topk * 4);
-    w.cnt = cv.take<int32_t>(C * c.E * 4);
+    w.cnt = cv.take<int32_t>(std::max<size_t>(C, 1) * c.E * 4);
     w.counts = cv.take<int32_t>(static_cast<size_t>(c.E) * 4);
     w.offsets = cv.take<int32_t>(static_cast<size_t>(c.E + 1) * 4);
     w.sorted_tok = cv.take<int32_t>(Tz * c.topk * 4);
     w.inv_pos = cv.take<int32_t>(Tz * c.topk * 4);
     w.row_start = cv.take<int32_t>((G + 1) * 4);
     w.tile_prefix = cv.take<int32_t>((G + 1) * 4);
+    w.tile_prefix_dn = cv.take<int32_t>((G + 1) * 4);
+    w.counters = cv.take<int32_t>(2 * 4);
     w.xq_perm = cv.take<uint8_t>(R * c.d);
     w.sx_perm = cv.take<float>(R * (c.d / 128) * 4);
     w.hq = cv.take<uint8_t>(R * c.H);
@@ -183,6 +217,7 @@ int make_map(CUtensorMap *m, const void *ptr, int elem_bytes, uint64_t rows, uin
 
 int route_impl(const void *x, const void *wg, const float *bias, const moe_cfg_t &c, int T, int32_t *idx,
                float *w, float *scores, float *logits, cudaStream_t st) {
+    const int bn = router_bn(T);
     CUtensorMap ma, mb;
     MOE_CHECK(make_map(&ma, wg, 2, c.E, c.d, kBM));
     MOE_CHECK(make_map(&mb, x, 2, T, c.d, kActBoxRows));
@@ -194,9 +229,10 @@ int route_impl(const void *x, const void *wg, const float *bias, const moe_cfg_t
     a.single_rows = T;
     a.logits = logits;
     a.n_valid = c.E;
-    const int items = a.num_mb * ((T + kBN - 1) / kBN);
-    MOE_CUDA(launch_grouped_gemm(Kind::Router, ma, mb, a, std::min(items, num_sms()), st), "router GEMM launch");
-    MOE_CUDA(launch_topk(logits, bias, T, c.E, c.topk, c.route_scale, idx, w, scores, st), "top-k launch");
+    a.k_splits = router_splits(c, T);
+    const int items = a.num_mb * ((T + bn - 1) / bn) * a.k_splits;
+    MOE_CUDA(launch_grouped_gemm(Kind::Router, bn, ma, mb, a, std::min(items, num_sms()), st), "router GEMM launch");
+    MOE_CUDA(launch_topk(logits, a.k_splits, bias, T, c.E, c.topk, c.route_scale, idx, w, scores, st), "top-k launch");
     t_launches += 2;
     return MOE_OK;
 }
@@ -206,8 +242,10 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
                 bool run_sched, cudaStream_t st) {
     const int G = c.E + c.n_shared;
     const int64_t R = static_cast<int64_t>(c.topk + c.n_shared) * T;
+    const int bn = expert_bn(c, T);
     if (run_sched) {
-        MOE_CUDA(launch_sched(offsets, c.E, c.n_shared, T, c.topk, kBN, ws.row_start, ws.tile_prefix, st),
+        MOE_CUDA(launch_sched(offsets, c.E, c.n_shared, T, c.topk, bn, down_bn(c, T), ws.row_start, ws.tile_prefix,
+                              ws.tile_prefix_dn, ws.counters, st),
                  "schedule launch");
         t_launches += 1;
     }
@@ -222,13 +260,14 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     gu.single_rows = -1;
     gu.row_start = ws.row_start;
     gu.tile_prefix = ws.tile_prefix;
+    gu.item_counter = ws.counters;
     gu.act_scale_t = sx_perm;
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * c.H;
     gu.a_second_offset = c.H;
     gu.hq = hq;
     gu.hs_t = hs;
-    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, bn, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
     t_launches += 1;
     return MOE_OK;
 }
@@ -237,8 +276,10 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
               const moe_cfg_t &c, int T, void *o, const LayerWs &ws, bool run_sched, cudaStream_t st) {
     const int G = c.E + c.n_shared;
     const int64_t R = static_cast<int64_t>(c.topk + c.n_shared) * T;
+    const int bn = down_bn(c, T);
     if (run_sched) {
-        MOE_CUDA(launch_sched(offsets, c.E, c.n_shared, T, c.topk, kBN, ws.row_start, ws.tile_prefix, st),
+        MOE_CUDA(launch_sched(offsets, c.E, c.n_shared, T, c.topk, expert_bn(c, T), bn, ws.row_start,
+                              ws.tile_prefix, ws.tile_prefix_dn, ws.counters, st),
                  "schedule launch");
         t_launches += 1;
     }
@@ -252,20 +293,21 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
     dn.total_rows = static_cast<int>(R);
     dn.single_rows = -1;
     dn.row_start = ws.row_start;
-    dn.tile_prefix = ws.tile_prefix;
+    dn.tile_prefix = ws.tile_prefix_dn;
+    dn.item_counter = ws.counters + 1;
     dn.act_scale_t = hs;
     dn.w_scale = w2_s;
     dn.a_rows_per_group = c.d;
     dn.out = static_cast<__nv_bfloat16 *>(o);
-    MOE_CUDA(launch_grouped_gemm(Kind::Down, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::Down, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     t_launches += 1;
     return MOE_OK;
 }
 
 int experts_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets, const uint8_t *w13,
                  const float *w13_s, const uint8_t *w2, const float *w2_s, const moe_cfg_t &c, int T, void *o,
-                 const LayerWs &ws, cudaStream_t st) {
-    MOE_CHECK(gateup_impl(xq_perm, sx_perm, offsets, w13, w13_s, c, T, ws.hq, ws.hs_t, ws, true, st));
+                 const LayerWs &ws, bool run_sched, cudaStream_t st) {
+    MOE_CHECK(gateup_impl(xq_perm, sx_perm, offsets, w13, w13_s, c, T, ws.hq, ws.hs_t, ws, run_sched, st));
     return down_impl(ws.hq, ws.hs_t, offsets, w2, w2_s, c, T, o, ws, false, st);
 }
 
@@ -335,8 +377,9 @@ int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx, con
     MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
     const LayerWs ws = carve_layer(*cfg, T, workspace);
     int n = 0;
-    MOE_CUDA(launch_permute(topk_idx, xq, sx, T, cfg->topk, cfg->n_shared, cfg->E, cfg->d, ws.rank, ws.cnt,
-                            ws.counts, offsets, sorted_tok, inv_pos, xq_perm, sx_perm, &n,
+    MOE_CUDA(launch_permute(topk_idx, xq, sx, T, cfg->topk, cfg->n_shared, cfg->E, cfg->d, expert_bn(*cfg, T),
+                            down_bn(*cfg, T), ws.rank, ws.cnt, ws.counts, offsets, ws.row_start, ws.tile_prefix,
+                            ws.tile_prefix_dn, ws.counters, sorted_tok, inv_pos, xq_perm, sx_perm, &n,
                             static_cast<cudaStream_t>(stream)),
              "permutation launch");
     t_launches = n;
@@ -361,7 +404,7 @@ int moe_expert_gemm_fp8(const uint8_t *xq_perm, const float *sx_perm, const int3
     const LayerWs need = carve_layer(*cfg, T, nullptr);
     MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
     const LayerWs ws = carve_layer(*cfg, T, workspace);
-    return experts_impl(xq_perm, sx_perm, offsets, w13, w13_s, w2, w2_s, *cfg, T, o, ws,
+    return experts_impl(xq_perm, sx_perm, offsets, w13, w13_s, w2, w2_s, *cfg, T, o, ws, true,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -452,12 +495,14 @@ int moe_layer_forward(const void *x, const void *w_gate, const float *bias, cons
     MOE_CUDA(launch_quant(x, true, T, c.d, ws.xq, ws.sx, false, num_sms(), st), "quantise launch");
     n += 1;
     int np = 0;
-    MOE_CUDA(launch_permute(idx, ws.xq, ws.sx, T, c.topk, c.n_shared, c.E, c.d, ws.rank, ws.cnt, ws.counts,
-                            ws.offsets, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st),
+    MOE_CUDA(launch_permute(idx, ws.xq, ws.sx, T, c.topk, c.n_shared, c.E, c.d, expert_bn(c, T), down_bn(c, T),
+                            ws.rank, ws.cnt, ws.counts, ws.offsets, ws.row_start, ws.tile_prefix, ws.tile_prefix_dn,
+                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st),
              "permutation launch");
     n += np;
     t_launches = 0;
-    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, st));
+    // the permutation already wrote the GEMM schedule into the workspace
+    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, false, st));
     n += t_launches;
     MOE_CUDA(launch_combine(ws.o, w, ws.inv_pos, T, c.topk, c.n_shared, c.d, y, st), "combine launch");
     n += 1;
@@ -515,7 +560,7 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     gu.a_second_offset = H;
     gu.hq = hq;
     gu.hs_t = hs_t;
-    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, 64, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
     GemmArgs dn{};
     dn.G = 1;
     dn.num_kb = H / 128;
@@ -526,7 +571,7 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     dn.w_scale = w2_s;
     dn.a_rows_per_group = d;
     dn.out = static_cast<__nv_bfloat16 *>(y);
-    MOE_CUDA(launch_grouped_gemm(Kind::Down, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::Down, 128, m2, mh, dn, num_sms(), st), "down GEMM launch");
     t_launches = 3;
     return MOE_OK;
 }

@@ -10,26 +10,40 @@ cudaError_t device_error_word(unsigned int **ptr) {
     return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_moe_device_error);
 }
 
-template <Kind KIND>
+template <Kind KIND, int BN>
 static cudaError_t launch_kind(const CUtensorMap &map_a, const CUtensorMap &map_b, const GemmArgs &args,
                                int grid, cudaStream_t stream) {
-    constexpr size_t smem = gemm_smem_bytes<KIND>();
-    static_assert(smem <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr size_t smem = gemm_smem_bytes<KIND, BN>();
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<KIND><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
+    grouped_gemm_kernel<KIND, BN><<<grid, KindCfg<KIND, BN>::kThreads, smem, stream>>>(map_a, map_b, args);
     return cudaGetLastError();
 }
 
-cudaError_t launch_grouped_gemm(Kind kind, const CUtensorMap &map_a, const CUtensorMap &map_b, GemmArgs &args,
-                                int grid, cudaStream_t stream) {
+// Token-tile widths compiled per kind: the gate/up epilogue holds two
+// accumulators per column, so it stops at 64-token tiles.
+template <Kind KIND>
+static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const CUtensorMap &map_b, const GemmArgs &args,
+                             int grid, cudaStream_t stream) {
+    switch (bn) {
+        case 32: return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
+        case 64: return launch_kind<KIND, 64>(map_a, map_b, args, grid, stream);
+        case 128:
+            if constexpr (KIND != Kind::GateUp) return launch_kind<KIND, 128>(map_a, map_b, args, grid, stream);
+            break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                GemmArgs &args, int grid, cudaStream_t stream) {
     cudaError_t e = device_error_word(&args.err);
     if (e != cudaSuccess) return e;
     switch (kind) {
-        case Kind::GateUp: return launch_kind<Kind::GateUp>(map_a, map_b, args, grid, stream);
-        case Kind::Down: return launch_kind<Kind::Down>(map_a, map_b, args, grid, stream);
-        case Kind::Router: return launch_kind<Kind::Router>(map_a, map_b, args, grid, stream);
+        case Kind::GateUp: return launch_bn<Kind::GateUp>(bn, map_a, map_b, args, grid, stream);
+        case Kind::Down: return launch_bn<Kind::Down>(bn, map_a, map_b, args, grid, stream);
+        case Kind::Router: return launch_bn<Kind::Router>(bn, map_a, map_b, args, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -6,19 +6,28 @@
 // token tile nt); items of one group are ordered mb-major so that the token
 // tiles sharing a weight block run at the same time on neighbouring CTAs.
 //
-// Roles (320 threads, one CTA per SM):
-//   warp 0      TMA producer: weight tile(s) + activation rows per 128-byte K block
+// Roles (one CTA per SM):
+//   warp 0      producer: takes work items from the tile scheduler, issues the
+//               TMA tile loads (weight tile(s) + activation rows per 128-byte K
+//               block) and copies the scales of each stage
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..9  epilogue: two groups of four warps, one per half of the token
-//               columns; each warp reads its 32-lane quarter of TMEM
+//   warps 2..   epilogue: 2 or 4 column groups of four warps; each warp reads
+//               its 32-lane quarter of TMEM for its group's token columns
+//
+// Tile scheduler: for expert groups the producer takes the next item from a
+// global counter (atomicAdd), so token tiles that share a weight block start
+// within a microsecond of each other on whichever CTAs are free (their weight
+// tiles are then read from HBM once), and unequal items balance themselves.
+// Single-group GEMMs (router, dense FFN) use a static round-robin order. The
+// item index reaches the MMA and epilogue warps through a shared-memory queue.
 //
 // FP8 kinds (gate/up and down): e4m3 x e4m3 -> fp32 with one partial product
 // per 128-wide K block, because the weight scale (per 128x128 block) and the
 // activation scale (per token and 128-wide K block) both change at every K
 // block. The epilogue promotes each partial into fp32 registers:
 //     acc[j] += (s_w[mb, kb] * s_x[row_j, kb]) * partial[j]
-// TMEM holds two partial buffers so the MMAs of K block kb+1 run while block
-// kb is promoted.
+// TMEM holds two to four partial buffers so the MMAs of the next K blocks run
+// while block kb is promoted.
 //
 // Router kind: bf16 x bf16 -> fp32, accumulated in TMEM over the whole K
 // range; the epilogue writes fp32 logits.
@@ -29,28 +38,40 @@ namespace moe {
 
 enum class Kind { GateUp, Down, Router };
 
-constexpr int kBN = 128;                    // max tokens per tile (MMA N)
 constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
 constexpr int kATileBytes = kBM * kKBytes;  // 16 KB
-constexpr int kBTileBytes = kBN * kKBytes;  // 16 KB
 constexpr int kActBoxRows = 16;             // activation TMA box height
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
 constexpr int kMaxGroups = 1032;            // routed + shared experts, padded
+constexpr int kItemQ = 4;                   // depth of the producer -> consumers item queue
 
-template <Kind K> struct KindCfg;
-template <> struct KindCfg<Kind::GateUp> {
-    static constexpr int kATiles = 2, kStages = 4, kTmemCols = 512, kPartCols = 256;
-    static constexpr bool kPromote = true, kBf16 = false;
-};
-template <> struct KindCfg<Kind::Down> {
-    static constexpr int kATiles = 1, kStages = 6, kTmemCols = 256, kPartCols = 128;
-    static constexpr bool kPromote = true, kBf16 = false;
-};
-template <> struct KindCfg<Kind::Router> {
-    static constexpr int kATiles = 1, kStages = 6, kTmemCols = 256, kPartCols = 128;
-    static constexpr bool kPromote = false, kBf16 = true;
+constexpr int kStageBudget = 200 * 1024;    // shared memory for the operand ring
+
+constexpr int pow2_at_least(int v, int lo) { return v <= lo ? lo : 2 * pow2_at_least((v + 1) / 2, lo); }
+
+// Per-kind, per-tile-width configuration. BN = tokens per tile (MMA N upper bound).
+template <Kind K, int BN> struct KindCfg {
+    static constexpr int kATiles = (K == Kind::GateUp) ? 2 : 1;   // gate and up weight tiles
+    static constexpr bool kPromote = (K != Kind::Router);         // per-128-K fp32 promotion
+    static constexpr bool kBf16 = (K == Kind::Router);
+    static constexpr int kBTileBytes = BN * kKBytes;
+    static constexpr int kStageBytes = kATiles * kATileBytes + kBTileBytes;
+    static constexpr int kStages = (kStageBudget / kStageBytes) > 12 ? 12 : (kStageBudget / kStageBytes);
+    static constexpr int kPartCols = kATiles * BN;                // one TMEM partial buffer
+    // partial buffers in flight between the MMA issuer and the epilogue: as
+    // many as TMEM holds, up to 4, so the MMAs run ahead of the promotion
+    static constexpr int kNumPart = (512 / kPartCols) >= 4 ? 4 : (512 / kPartCols);
+    static constexpr int kTmemCols = pow2_at_least(kNumPart * kPartCols, 32);
+    // scale slots: their own ring, released by the epilogue, so operand stages
+    // are released by the MMA alone and the producer keeps kStages ahead of it
+    static constexpr int kScaleSlots = kPromote ? (kStages + kNumPart + 2) : 1;
+    static constexpr int kGroups = 2;                             // epilogue column groups
+    static constexpr int kHalfCols = BN / kGroups;                // token columns per column group
+    static constexpr int kChunks = kHalfCols / 16;
+    static constexpr int kEpiWarps = 4 * kGroups;                 // one warp per TMEM lane quarter and group
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
+    static_assert(kStages >= 3, "pipeline depth");
 };
 
 struct GemmArgs {
@@ -60,7 +81,7 @@ struct GemmArgs {
     int total_rows;           // rows of the activation buffer
     int single_rows;          // >= 0: one group of that many rows (row_start / tile_prefix unused)
     const int *row_start;     // [G+1] first activation row of each group's segment
-    const int *tile_prefix;   // [G+1] prefix sum of ceil(rows_g / kBN)
+    const int *tile_prefix;   // [G+1] prefix sum of ceil(rows_g / BN)
     const float *act_scale_t; // [num_kb][total_rows]  (FP8 kinds)
     const float *w_scale;     // GateUp: [G][2][num_mb][num_kb]; Down: [G][num_mb][num_kb]
     int a_rows_per_group;     // weight rows of one group in the A tensor map (GateUp: 2*H, Down: d_out)
@@ -68,26 +89,36 @@ struct GemmArgs {
     uint8_t *hq;              // GateUp: [total_rows][num_mb*128]
     float *hs_t;              // GateUp: [num_mb][total_rows]
     __nv_bfloat16 *out;       // Down: [total_rows][num_mb*128]
-    float *logits;            // Router: [total_rows][n_valid]
+    float *logits;            // Router: [k_splits][total_rows][n_valid] partial logits
     int n_valid;              // Router: valid weight rows (experts)
+    int k_splits;             // Router: K range split into this many partial sums (>= 1)
     unsigned int *err;        // device error word (bounded waits that gave up)
+    int *item_counter;        // dynamic scheduler counter (zero at launch), or null for static order
 };
 
 struct Item {
-    int g, mb, row0, n;
+    int g, mb, row0, n, ks;
+    int ntiles;   // token tiles of the item's group (tiles sharing its weight block)
 };
 
+template <int BN>
 __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int *s_tp,
                                             const int *s_rs, Item &o) {
     if (a.single_rows >= 0) {
-        const int nt_total = (a.single_rows + kBN - 1) / kBN;
+        // items = (mb, token tile, K split) with the split fastest
+        const int nt_total = (a.single_rows + BN - 1) / BN;
+        const int splits = a.k_splits > 0 ? a.k_splits : 1;
+        o.ks = it % splits;
+        const int rest = it / splits;
         o.g = 0;
-        o.mb = it / nt_total;
-        const int nt = it - o.mb * nt_total;
-        o.row0 = nt * kBN;
-        o.n = min(kBN, a.single_rows - o.row0);
+        o.mb = rest / nt_total;
+        const int nt = rest - o.mb * nt_total;
+        o.row0 = nt * BN;
+        o.n = min(BN, a.single_rows - o.row0);
+        o.ntiles = nt_total;
         return o.n > 0 && o.mb < a.num_mb;
     }
+    o.ks = 0;
     const int key = it / a.num_mb;
     int lo = 0, hi = a.G;  // find the last g with tile_prefix[g] <= key
     while (hi - lo > 1) {
@@ -101,60 +132,82 @@ __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int
     o.g = g;
     o.mb = li / nt_g;
     const int nt = li - o.mb * nt_g;
-    o.row0 = s_rs[g] + nt * kBN;
-    o.n = min(kBN, s_rs[g + 1] - o.row0);
+    o.row0 = s_rs[g] + nt * BN;
+    o.n = min(BN, s_rs[g + 1] - o.row0);
+    o.ntiles = nt_g;
     return o.n > 0 && o.mb < a.num_mb;
 }
 
+template <int BN>
 __device__ __forceinline__ int total_items(const GemmArgs &a, const int *s_tp) {
-    if (a.single_rows >= 0) return a.num_mb * ((a.single_rows + kBN - 1) / kBN);
+    if (a.single_rows >= 0)
+        return a.num_mb * ((a.single_rows + BN - 1) / BN) * (a.k_splits > 0 ? a.k_splits : 1);
     return a.num_mb * s_tp[a.G];
+}
+
+// K blocks [kb0, kb1) of one item.
+__device__ __forceinline__ void kb_range(const GemmArgs &a, const Item &I, int &kb0, int &kb1) {
+    const int splits = a.k_splits > 0 ? a.k_splits : 1;
+    kb0 = (a.num_kb * I.ks) / splits;
+    kb1 = (a.num_kb * (I.ks + 1)) / splits;
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // Shared-memory carve-up of one CTA (offsets from a 1024-byte aligned base).
-template <Kind KIND> struct SmemLayout {
-    using C = KindCfg<KIND>;
-    static constexpr int kStageBytes = C::kATiles * kATileBytes + kBTileBytes;
-    static constexpr int kNumBars = 2 * C::kStages + 2 + 2 + 1 + 4;
-    static constexpr size_t kBars = static_cast<size_t>(C::kStages) * kStageBytes;
+template <Kind KIND, int BN> struct SmemLayout {
+    using C = KindCfg<KIND, BN>;
+    static constexpr int kNumBars = 2 * C::kStages + 2 * C::kNumPart + 1 + 2 * C::kGroups + 2 * kItemQ +
+                                    2 * C::kScaleSlots;
+    static constexpr size_t kBars = static_cast<size_t>(C::kStages) * C::kStageBytes;
     static constexpr size_t kMisc = (kBars + kNumBars * 8 + 15) & ~size_t(15);
-    static constexpr size_t kTp = kMisc + 16;
+    static constexpr size_t kItems = kMisc + 16;                                // [kItemQ] int
+    static constexpr size_t kTp = kItems + kItemQ * 4;
     static constexpr size_t kRs = kTp + kMaxGroups * 4;
-    static constexpr size_t kScale = kRs + kMaxGroups * 4;
-    static constexpr size_t kAmax = kScale + kEpiWarps * 2 * 64 * 4;
-    static constexpr size_t kEnd = kAmax + 2 * 2 * 4 * 64 * 4;
+    static constexpr int kScaleStride = BN + 4;                                // floats per stage: BN act + 2 weight
+    static constexpr size_t kScale = kRs + kMaxGroups * 4;                     // [kScaleSlots][kScaleStride]
+    static constexpr size_t kCs = kScale + C::kScaleSlots * kScaleStride * 4;  // [warps][2][kATiles][HC]
+    static constexpr size_t kAmax = kCs + C::kEpiWarps * 2 * C::kATiles * C::kHalfCols * 4;  // [groups][2][4][HC]
+    static constexpr size_t kEnd = kAmax + C::kGroups * 2 * 4 * C::kHalfCols * 4;
     static constexpr size_t kLaunchBytes = kEnd + 1024;  // + alignment slack of the dynamic base
-    static_assert(kBars % 1024 == 0 && kScale % 16 == 0, "alignment");
+    static_assert(kBars % 1024 == 0 && kScale % 16 == 0 && kCs % 16 == 0, "alignment");
+    static_assert(kLaunchBytes <= 232448, "shared memory budget");
 };
 
-template <Kind KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+template <Kind KIND, int BN>
+__global__ void __launch_bounds__(KindCfg<KIND, BN>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const GemmArgs args) {
-    using C = KindCfg<KIND>;
-    constexpr int kStageBytes = SmemLayout<KIND>::kStageBytes;
+    using C = KindCfg<KIND, BN>;
+    using L = SmemLayout<KIND, BN>;
+    constexpr int kStageBytes = C::kStageBytes;
     constexpr int kKbElems = C::kBf16 ? 64 : 128;
     constexpr uint32_t kFmt = C::kBf16 ? 1u : 0u;
+    constexpr int HC = C::kHalfCols;
+    constexpr int kEpi = C::kEpiWarps;
 
     extern __shared__ uint8_t smem_raw[];
-    using L = SmemLayout<KIND>;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *full = bars;
     uint64_t *empty = full + C::kStages;
     uint64_t *pfull = empty + C::kStages;
-    uint64_t *pempty = pfull + 2;
-    uint64_t *mma_done = pempty + 2;
-    uint64_t *amax_bar = mma_done + 1;  // [2 halves][2 buffers]
+    uint64_t *pempty = pfull + C::kNumPart;
+    uint64_t *mma_done = pempty + C::kNumPart;
+    uint64_t *amax_bar = mma_done + 1;                  // [groups][2 buffers]
+    uint64_t *item_full = amax_bar + 2 * C::kGroups;     // [kItemQ]
+    uint64_t *item_empty = item_full + kItemQ;           // [kItemQ]
+    uint64_t *sfull = item_empty + kItemQ;               // [kScaleSlots]
+    uint64_t *sempty = sfull + C::kScaleSlots;           // [kScaleSlots]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *s_items = reinterpret_cast<volatile int *>(smem + L::kItems);
     int *s_tp = reinterpret_cast<int *>(smem + L::kTp);
     int *s_rs = reinterpret_cast<int *>(smem + L::kRs);
-    float *s_scale = reinterpret_cast<float *>(smem + L::kScale);  // [8 warps][2][64]
-    float *s_amax = reinterpret_cast<float *>(smem + L::kAmax);    // [2 halves][2 bufs][4 quads][64]
+    float *s_scale = reinterpret_cast<float *>(smem + L::kScale);  // scale slots
+    float *s_cs = reinterpret_cast<float *>(smem + L::kCs);        // per-warp combined scales
+    float *s_amax = reinterpret_cast<float *>(smem + L::kAmax);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -167,15 +220,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&full[s]), 1);    // the producer's expect_tx arrival (+ TMA bytes)
+            mbar_init(smem_u32(&empty[s]), 1);   // the MMA commit
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int s = 0; s < C::kScaleSlots; ++s) {
+            mbar_init(smem_u32(&sfull[s]), 32);    // one cp.async arrival per producer lane
+            mbar_init(smem_u32(&sempty[s]), kEpi); // one arrival per epilogue warp
+        }
+        for (int b = 0; b < C::kNumPart; ++b) {
             mbar_init(smem_u32(&pfull[b]), 1);
-            mbar_init(smem_u32(&pempty[b]), kEpiWarps);
+            mbar_init(smem_u32(&pempty[b]), kEpi);
         }
         mbar_init(smem_u32(mma_done), 1);
-        for (int b = 0; b < 4; ++b) mbar_init(smem_u32(&amax_bar[b]), 4);
+        for (int b = 0; b < 2 * C::kGroups; ++b) mbar_init(smem_u32(&amax_bar[b]), 4);
+        for (int b = 0; b < kItemQ; ++b) {
+            mbar_init(smem_u32(&item_full[b]), 1);
+            mbar_init(smem_u32(&item_empty[b]), 1 + kEpi);
+        }
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&map_a);
@@ -186,52 +247,119 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int n_items = total_items(args, s_tp);
+    const int n_items = total_items<BN>(args, s_tp);
+
+    // Next item for a consumer: wait for the producer's queue slot, read it,
+    // release the slot. Called by lane 0; returns -1 on give-up.
+    auto take_item = [&](int &q, uint32_t &qphase) -> int {
+        if (!mbar_wait(smem_u32(&item_full[q]), qphase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) return -1;
+        const int it = s_items[q];
+        mbar_arrive(smem_u32(&item_empty[q]));
+        if (++q == kItemQ) { q = 0; qphase ^= 1; }
+        return it;
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_x = policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;
-            bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                Item I;
-                if (!decode_item(it, args, s_tp, s_rs, I)) { record_error(args.err, ERR_BAD_TILE); continue; }
-                const int nb16 = (I.n + kActBoxRows - 1) / kActBoxRows;
-                const uint32_t bytes = C::kATiles * kATileBytes + nb16 * kActBoxRows * kKBytes;
-                int arow0, arow1 = 0;
-                if (KIND == Kind::Router) {
-                    arow0 = I.mb * kBM;
-                } else {
-                    arow0 = I.g * args.a_rows_per_group + I.mb * kBM;
-                    arow1 = arow0 + args.a_second_offset;
+        // ------------------------------------------------------------ producer
+        // lane 0 fetches items and issues the TMA tile loads; all lanes copy the
+        // stage's scales (activation scales of the tile's tokens, weight scales)
+        // weights read by one token tile only are streamed (evict first); a weight
+        // block shared by several token tiles, which run at the same time, stays
+        // in L2 for them (normal policy)
+        const uint64_t pol_stream = policy_evict_first();
+        const uint64_t pol_shared = policy_evict_normal();
+        const uint64_t pol_x = policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        int sslot = 0;
+        uint32_t sphase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        int q = 0;
+        uint32_t qphase = 0;
+        int next_static = blockIdx.x;
+        while (true) {
+            int it = 0, got = 1;
+            if (lane == 0) {
+                got = mbar_wait(smem_u32(&item_empty[q]), qphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
+                if (got) {
+                    if (args.item_counter) it = atomicAdd(args.item_counter, 1);
+                    else { it = next_static; next_static += gridDim.x; }
+                    if (it > n_items) it = n_items;
+                    s_items[q] = it;
+                    mbar_arrive(smem_u32(&item_full[q]));
                 }
-                for (int kb = 0; kb < args.num_kb; ++kb) {
-                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = smem_u32(&full[stage]);
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            it = __shfl_sync(0xffffffffu, it, 0);
+            if (!got || it >= n_items) break;
+            if (++q == kItemQ) { q = 0; qphase ^= 1; }
+            Item I;
+            if (!decode_item<BN>(it, args, s_tp, s_rs, I)) {
+                if (lane == 0) record_error(args.err, ERR_BAD_TILE);
+                continue;
+            }
+            int kb0, kb1;
+            kb_range(args, I, kb0, kb1);
+            const int nb16 = (I.n + kActBoxRows - 1) / kActBoxRows;
+            const uint32_t bytes = C::kATiles * kATileBytes + nb16 * kActBoxRows * kKBytes;
+            const uint64_t pol_w = (I.ntiles > 1) ? pol_shared : pol_stream;
+            int arow0, arow1 = 0;
+            const float *ws0 = nullptr, *ws1 = nullptr;
+            if constexpr (KIND == Kind::Router) {
+                arow0 = I.mb * kBM;
+            } else {
+                arow0 = I.g * args.a_rows_per_group + I.mb * kBM;
+                arow1 = arow0 + args.a_second_offset;
+                if constexpr (KIND == Kind::GateUp) {
+                    ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
+                    ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
+                } else {
+                    ws0 = args.w_scale + (static_cast<size_t>(I.g) * args.num_mb + I.mb) * args.num_kb;
+                }
+            }
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                int w = 1;
+                if (lane == 0) {
+                    w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
+                    if (C::kPromote && w)
+                        w = mbar_wait(smem_u32(&sempty[sslot]), sphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
+                }
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) { ok = false; break; }
+                const uint32_t fb = smem_u32(&full[stage]);
+                const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
+                if (lane == 0) {
                     mbar_arrive_expect_tx(fb, bytes);
-                    const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
                     const int kx = kb * kKbElems;
                     tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
-                    if (C::kATiles == 2) tma_load_2d(sbase + kATileBytes, &map_a, fb, kx, arow1, pol_w);
+                    if constexpr (C::kATiles == 2) tma_load_2d(sbase + kATileBytes, &map_a, fb, kx, arow1, pol_w);
                     const uint32_t bdst = sbase + C::kATiles * kATileBytes;
                     for (int i = 0; i < nb16; ++i)
                         tma_load_2d(bdst + i * kActBoxRows * kKBytes, &map_b, fb, kx, I.row0 + i * kActBoxRows, pol_x);
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
+                if constexpr (C::kPromote) {
+                    const uint32_t sdst = smem_u32(s_scale + sslot * L::kScaleStride);
+                    const float *src = args.act_scale_t + static_cast<size_t>(kb) * args.total_rows + I.row0;
+                    for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
+                    if (lane == 0) {
+                        cp_async_4(sdst + 4 * BN, ws0 + kb);
+                        if constexpr (KIND == Kind::GateUp) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
+                    }
+                    cp_async_arrive_noinc(smem_u32(&sfull[sslot]));
+                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
+                }
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == C::kStages) { stage = 0; phase ^= 1; }
             }
-            // every issued copy must land before the CTA may exit
+            if (!ok) break;
+        }
+        // every issued copy must land before the CTA may exit
+        if constexpr (C::kPromote) cp_async_wait_all();
+        if (lane == 0)
             for (int s = 0; s < C::kStages; ++s)
                 if (issued_mask & (1u << s)) mbar_wait_drain(smem_u32(&full[s]), (issued_parity >> s) & 1u, args.err);
-        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -239,15 +367,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             uint32_t phase = 0;
             int pbuf = 0;
             uint32_t pphase = 0;
+            int q = 0;
+            uint32_t qphase = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            while (ok) {
+                const int it = take_item(q, qphase);
+                if (it < 0 || it >= n_items) break;
                 Item I;
-                if (!decode_item(it, args, s_tp, s_rs, I)) continue;
+                if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
+                int kb0, kb1;
+                kb_range(args, I, kb0, kb1);
                 const int n_mma = (I.n + 15) & ~15;
                 const uint32_t idesc = idesc_make(kFmt, kFmt, kBM, n_mma);
-                for (int kb = 0; kb < args.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) { ok = false; break; }
-                    if (C::kPromote || kb == 0) {
+                    if (C::kPromote || kb == kb0) {
                         if (!mbar_wait(smem_u32(&pempty[pbuf]), pphase ^ 1, abort_flag, args.err, ERR_WAIT_PART_EMPTY)) {
                             ok = false;
                             break;
@@ -259,19 +393,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const uint32_t dcol = tmem_base + pbuf * C::kPartCols;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint32_t acc = C::kPromote ? (k > 0) : (kb > 0 || k > 0);
+                        const uint32_t acc = C::kPromote ? (k > 0) : (kb > kb0 || k > 0);
                         const uint64_t bdesc = sdesc_sw128(bbase + k * 32);
                         const uint64_t adesc = sdesc_sw128(sbase + k * 32);
                         if constexpr (C::kBf16) mma_bf16(dcol, adesc, bdesc, idesc, acc);
                         else mma_f8(dcol, adesc, bdesc, idesc, acc);
                         if constexpr (C::kATiles == 2)
-                            mma_f8(dcol + kBN, sdesc_sw128(sbase + kATileBytes + k * 32), bdesc, idesc, acc);
+                            mma_f8(dcol + BN, sdesc_sw128(sbase + kATileBytes + k * 32), bdesc, idesc, acc);
                     }
                     mma_commit(smem_u32(&empty[stage]));
-                    if (C::kPromote || kb == args.num_kb - 1) {
+                    if (C::kPromote || kb == kb1 - 1) {
                         mma_commit(smem_u32(&pfull[pbuf]));
-                        pbuf ^= 1;
-                        if (pbuf == 0) pphase ^= 1;
+                        if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
                     }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
@@ -284,83 +417,93 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;
         const int quad = warp & 3;           // TMEM lane quarter this warp may access
-        const int half = ew >> 2;            // token columns [64*half, 64*half + 64)
-        const int col_base = half * 64;
+        const int grp = ew >> 2;             // token columns [HC*grp, HC*grp + HC)
+        const int col_base = grp * HC;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-        float *my_scale = s_scale + ew * 2 * 64;
+        int sslot = 0;                       // scale slot of the K block being promoted
+        uint32_t sphase = 0;
         int pbuf = 0;
         uint32_t pphase = 0;
+        int q = 0;
+        uint32_t qphase = 0;
         int item_count = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        while (ok) {
+            int it = 0;
+            if (lane == 0) it = take_item(q, qphase);
+            it = __shfl_sync(0xffffffffu, it, 0);
+            if (it < 0 || it >= n_items) break;
             Item I;
-            if (!decode_item(it, args, s_tp, s_rs, I)) continue;
-            const int n_my = max(0, min(64, I.n - col_base));
+            if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
+            const int n_my = max(0, min(HC, I.n - col_base));
             if constexpr (C::kPromote) {
                 constexpr bool kTwo = (KIND == Kind::GateUp);
-                float acc0[64], acc1[kTwo ? 64 : 1];
+                float acc0[HC], acc1[HC];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) acc0[j] = 0.f;
-#pragma unroll
-                for (int j = 0; j < (kTwo ? 64 : 1); ++j) acc1[j] = 0.f;
-                const float *ws0, *ws1;
-                if constexpr (kTwo) {
-                    ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
-                    ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
-                } else {
-                    ws0 = args.w_scale + (static_cast<size_t>(I.g) * args.num_mb + I.mb) * args.num_kb;
-                    ws1 = ws0;
-                }
-                const float *sa_col = args.act_scale_t + I.row0 + col_base;
-                const size_t sa_stride = static_cast<size_t>(args.total_rows);
-                float pf0 = (lane < n_my) ? sa_col[lane] : 0.f;
-                float pf1 = (lane + 32 < n_my) ? sa_col[lane + 32] : 0.f;
-                float wr0 = 0.f, wr1 = 0.f;
+                for (int j = 0; j < HC; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
                 for (int kb = 0; kb < args.num_kb; ++kb) {
-                    float *slot = my_scale + (kb & 1) * 64;
-                    slot[lane] = pf0;
-                    slot[lane + 32] = pf1;
-                    if ((kb & 31) == 0) {
-                        wr0 = (kb + lane < args.num_kb) ? ws0[kb + lane] : 0.f;
-                        wr1 = (kb + lane < args.num_kb) ? ws1[kb + lane] : 0.f;
-                    }
-                    __syncwarp();
-                    if (kb + 1 < args.num_kb) {
-                        const float *nxt = sa_col + (kb + 1) * sa_stride;
-                        pf0 = (lane < n_my) ? nxt[lane] : 0.f;
-                        pf1 = (lane + 32 < n_my) ? nxt[lane + 32] : 0.f;
-                    }
-                    const float sw0 = __shfl_sync(0xffffffffu, wr0, kb & 31);
-                    const float sw1 = __shfl_sync(0xffffffffu, wr1, kb & 31);
+                    // 1. wait for this K block's partial products, start loading them
                     if (!mbar_wait(smem_u32(&pfull[pbuf]), pphase, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t tcol = t_lane + pbuf * C::kPartCols + col_base;
+                    float p[C::kATiles][C::kChunks][16];
+                    if (n_my > 0) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c * 16 < n_my) {
-                            float p0[16], p1[16];
-                            tmem_ld16(tcol + c * 16, p0);
-                            if constexpr (kTwo) tmem_ld16(tcol + kBN + c * 16, p1);
-                            tmem_wait_ld();
-                            const float4 *sv = reinterpret_cast<const float4 *>(slot + c * 16);
+                        for (int pass = 0; pass < C::kATiles; ++pass)
 #pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const float4 s4 = sv[v];
-                                const float sa[4] = {s4.x, s4.y, s4.z, s4.w};
+                            for (int c = 0; c < C::kChunks; ++c) tmem_ld16(tcol + pass * BN + c * 16, p[pass][c]);
+                    }
+                    // 2. while they are in flight: the combined scales
+                    //    s_w[mb, kb] * s_x[row_j, kb] of this warp's columns, once per
+                    //    K block, into a warp-private slot
+                    if (!mbar_wait(smem_u32(&sfull[sslot]), sphase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) {
+                        tmem_wait_ld();
+                        ok = false;
+                        break;
+                    }
+                    const float *sc = s_scale + sslot * L::kScaleStride;
+                    float *cs = s_cs + (ew * 2 + (kb & 1)) * C::kATiles * HC;
+                    {
+                        const float sw0 = sc[BN];
+                        const float sw1 = kTwo ? sc[BN + 1] : 0.f;
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int j = c * 16 + v * 4 + i;
-                                    acc0[j] = fmaf(sw0 * sa[i], p0[v * 4 + i], acc0[j]);
-                                    if constexpr (kTwo) acc1[j] = fmaf(sw1 * sa[i], p1[v * 4 + i], acc1[j]);
+                        for (int j = lane; j < HC; j += 32) {
+                            const float a = sc[col_base + j];
+                            cs[j] = sw0 * a;
+                            if constexpr (kTwo) cs[HC + j] = sw1 * a;
+                        }
+                    }
+                    __syncwarp();
+                    // 3. fold the partials into the fp32 accumulators
+                    if (n_my > 0) {
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int pass = 0; pass < C::kATiles; ++pass) {
+                            float *acc = (pass == 0) ? acc0 : acc1;
+                            const float *cp = cs + pass * HC;
+#pragma unroll
+                            for (int c = 0; c < C::kChunks; ++c) {
+                                const float4 *s4 = reinterpret_cast<const float4 *>(cp + c * 16);
+#pragma unroll
+                                for (int v = 0; v < 4; ++v) {
+                                    const float4 a4 = s4[v];
+                                    const int j = c * 16 + v * 4;
+                                    acc[j + 0] = fmaf(a4.x, p[pass][c][v * 4 + 0], acc[j + 0]);
+                                    acc[j + 1] = fmaf(a4.y, p[pass][c][v * 4 + 1], acc[j + 1]);
+                                    acc[j + 2] = fmaf(a4.z, p[pass][c][v * 4 + 2], acc[j + 2]);
+                                    acc[j + 3] = fmaf(a4.w, p[pass][c][v * 4 + 3], acc[j + 3]);
                                 }
                             }
                         }
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&pempty[pbuf]));
-                    pbuf ^= 1;
-                    if (pbuf == 0) pphase ^= 1;
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&pempty[pbuf]));
+                        mbar_arrive(smem_u32(&sempty[sslot]));
+                    }
+                    if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
+                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
                 }
                 if (!ok) break;
                 const int wrow = quad * 32 + lane;  // weight row inside the 128-row block
@@ -368,64 +511,49 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     // h = silu(g) * u, then 1x128 quantisation over the block's 128 rows
                     const int H = args.num_mb * kBM;
                     const int buf = item_count & 1;
-                    const uint32_t ab = smem_u32(&amax_bar[half * 2 + buf]);
-                    float *xch = s_amax + (half * 2 + buf) * 4 * 64;
+                    const uint32_t ab = smem_u32(&amax_bar[grp * 2 + buf]);
+                    float *xch = s_amax + (grp * 2 + buf) * 4 * HC;
+                    if (n_my > 0) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c * 16 < n_my) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int j = c * 16 + i;
-                                acc0[j] = silu_f(acc0[j]) * acc1[j];
-                                const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(acc0[j])));
-                                if (lane == 0) xch[quad * 64 + j] = __uint_as_float(m);
-                            }
+                        for (int j = 0; j < HC; ++j) {
+                            acc0[j] = silu_f(acc0[j]) * acc1[j];
+                            const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(acc0[j])));
+                            if (lane == 0) xch[quad * HC + j] = __uint_as_float(m);
                         }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(ab);
                     if (!mbar_wait(ab, (item_count >> 1) & 1, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c * 16 < n_my) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int j = c * 16 + i;
-                                if (j < n_my) {
-                                    const float amax = fmaxf(fmaxf(xch[j], xch[64 + j]), fmaxf(xch[128 + j], xch[192 + j]));
-                                    const float s = amax / 448.0f;
-                                    const uint8_t code = (amax == 0.f) ? uint8_t(0) : e4m3(acc0[j] / s);
-                                    const size_t row = static_cast<size_t>(I.row0 + col_base + j);
-                                    args.hq[row * H + I.mb * kBM + wrow] = code;
-                                    if (wrow == 0) args.hs_t[static_cast<size_t>(I.mb) * args.total_rows + row] = s;
-                                }
-                            }
+                    for (int j = 0; j < HC; ++j) {
+                        if (j < n_my) {
+                            const float amax = fmaxf(fmaxf(xch[j], xch[HC + j]), fmaxf(xch[2 * HC + j], xch[3 * HC + j]));
+                            const float s = amax / 448.0f;
+                            const uint8_t code = (amax == 0.f) ? uint8_t(0) : e4m3(acc0[j] / s);
+                            const size_t row = static_cast<size_t>(I.row0 + col_base + j);
+                            args.hq[row * H + I.mb * kBM + wrow] = code;
+                            if (wrow == 0) args.hs_t[static_cast<size_t>(I.mb) * args.total_rows + row] = s;
                         }
                     }
                 } else {
                     const int dout = args.num_mb * kBM;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c * 16 < n_my) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int j = c * 16 + i;
-                                if (j < n_my) {
-                                    const size_t row = static_cast<size_t>(I.row0 + col_base + j);
-                                    args.out[row * dout + I.mb * kBM + wrow] = __float2bfloat16_rn(acc0[j]);
-                                }
-                            }
+                    for (int j = 0; j < HC; ++j) {
+                        if (j < n_my) {
+                            const size_t row = static_cast<size_t>(I.row0 + col_base + j);
+                            args.out[row * dout + I.mb * kBM + wrow] = __float2bfloat16_rn(acc0[j]);
                         }
                     }
                 }
             } else {
-                // Router: one accumulator per item
+                // Router: one accumulator per item (one K split)
                 if (!mbar_wait(smem_u32(&pfull[pbuf]), pphase, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tcol = t_lane + pbuf * C::kPartCols + col_base;
                 const int e = I.mb * kBM + quad * 32 + lane;
+                float *dst = args.logits + static_cast<size_t>(I.ks) * args.total_rows * args.n_valid;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < C::kChunks; ++c) {
                     if (c * 16 < n_my) {
                         float p0[16];
                         tmem_ld16(tcol + c * 16, p0);
@@ -434,15 +562,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                         for (int i = 0; i < 16; ++i) {
                             const int j = c * 16 + i;
                             if (j < n_my && e < args.n_valid)
-                                args.logits[static_cast<size_t>(I.row0 + col_base + j) * args.n_valid + e] = p0[i];
+                                dst[static_cast<size_t>(I.row0 + col_base + j) * args.n_valid + e] = p0[i];
                         }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&pempty[pbuf]));
-                pbuf ^= 1;
-                if (pbuf == 0) pphase ^= 1;
+                if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
             }
             ++item_count;
         }
@@ -454,7 +581,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     if (warp == 1) tmem_dealloc<C::kTmemCols>(tmem_base);
 }
 
-template <Kind KIND>
-constexpr size_t gemm_smem_bytes() { return SmemLayout<KIND>::kLaunchBytes; }
+template <Kind KIND, int BN>
+constexpr size_t gemm_smem_bytes() { return SmemLayout<KIND, BN>::kLaunchBytes; }
 
 }  // namespace moe

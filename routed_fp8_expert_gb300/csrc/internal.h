@@ -10,7 +10,7 @@ struct GemmArgs;
 enum class Kind;
 
 // Grouped tcgen05 GEMM launch (gemm.cu). Returns a cudaError_t.
-cudaError_t launch_grouped_gemm(Kind kind, const CUtensorMap &map_a, const CUtensorMap &map_b,
+cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, const CUtensorMap &map_b,
                                 GemmArgs &args, int grid, cudaStream_t stream);
 // Address of the device error word on the current device (gemm.cu).
 cudaError_t device_error_word(unsigned int **ptr);
@@ -18,14 +18,17 @@ cudaError_t device_error_word(unsigned int **ptr);
 // Small kernels (kernels.cu).
 cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint8_t *q, float *s,
                          bool s_transposed, int num_sms, cudaStream_t stream);
-cudaError_t launch_topk(const float *logits, const float *bias, int T, int E, int k, float scale,
+cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream);
 cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *sx, int T, int k, int S, int E,
-                           int d, int32_t *rank, int32_t *cnt, int32_t *counts, int32_t *offsets,
-                           int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm, float *sx_perm,
-                           int *launches, cudaStream_t stream);
-cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile, int32_t *row_start,
-                         int32_t *tile_prefix, cudaStream_t stream);
+                           int d, int tile_a, int tile_b, int32_t *rank, int32_t *cnt, int32_t *counts,
+                           int32_t *offsets, int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b,
+                           int32_t *counters, int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm,
+                           float *sx_perm, int *launches,
+                           cudaStream_t stream);
+cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
+                         int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b, int32_t *counters,
+                         cudaStream_t stream);
 cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos, int T, int k, int S, int d,
                            void *y, cudaStream_t stream);
 

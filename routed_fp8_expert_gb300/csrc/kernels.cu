@@ -19,42 +19,49 @@ cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float *logits, const float *bias, int T, int E, int k, float scale,
+cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream) {
     const int threads = 256;  // 8 tokens per block
-    topk_kernel<<<(T + 7) / 8, threads, 0, stream>>>(logits, bias, T, E, k, scale, idx, w, scores);
+    topk_kernel<<<(T + 7) / 8, threads, 0, stream>>>(logits, splits, bias, T, E, k, scale, idx, w, scores);
     return cudaGetLastError();
 }
 
 cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *sx, int T, int k, int S, int E,
-                           int d, int32_t *rank, int32_t *cnt, int32_t *counts, int32_t *offsets,
-                           int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm, float *sx_perm,
-                           int *launches, cudaStream_t stream) {
+                           int d, int tile_a, int tile_b, int32_t *rank, int32_t *cnt, int32_t *counts,
+                           int32_t *offsets, int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b,
+                           int32_t *counters, int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm,
+                           float *sx_perm, int *launches,
+                           cudaStream_t stream) {
     const int C = (T + 31) / 32;
-    cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * static_cast<size_t>(E) * C, stream);
-    if (e != cudaSuccess) return e;
-    const size_t smem = sizeof(int32_t) * kPermWarps * 32 * k;
-    perm_rank_kernel<<<(C + kPermWarps - 1) / kPermWarps, kPermWarps * 32, smem, stream>>>(idx, T, k, C, rank, cnt);
+    const size_t smem = sizeof(uint32_t) * kPermWarps * E;
+    perm_rank_kernel<<<(C + kPermWarps - 1) / kPermWarps, kPermWarps * 32, smem, stream>>>(idx, T, k, E, C, rank,
+                                                                                            cnt);
     perm_scan_kernel<<<E, 256, 0, stream>>>(cnt, C, counts);
-    perm_offsets_kernel<<<1, 1024, 0, stream>>>(counts, E, offsets);
+    perm_offsets_kernel<<<1, 1024, 0, stream>>>(counts, E, S, T, k, tile_a, tile_b, offsets, row_start,
+                                                tile_prefix_a, tile_prefix_b, counters);
     const int threads = min(1024, max(64, d / 16));
-    perm_scatter_kernel<<<T, threads, 0, stream>>>(idx, rank, cnt, offsets, xq, sx, T, k, S, d, C, sorted_tok,
+    perm_scatter_kernel<<<T, threads, 0, stream>>>(idx, rank, cnt, offsets, xq, sx, T, k, S, E, d, C, sorted_tok,
                                                    inv_pos, xq_perm, sx_perm);
     *launches += 4;
     return cudaGetLastError();
 }
 
-cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile, int32_t *row_start,
-                         int32_t *tile_prefix, cudaStream_t stream) {
-    sched_kernel<<<1, 1024, 0, stream>>>(offsets, E, S, T, k, tile, row_start, tile_prefix);
+cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
+                         int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b, int32_t *counters,
+                         cudaStream_t stream) {
+    sched_kernel<<<1, 1024, 0, stream>>>(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a,
+                                         tile_prefix_b, counters);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos, int T, int k, int S, int d,
                            void *y, cudaStream_t stream) {
-    const int threads = min(256, max(32, d / 8));
-    combine_kernel<<<T, threads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d,
-                                              static_cast<__nv_bfloat16 *>(y));
+    // 128 threads x 8 features per block: a d=7168 token spans 7 blocks
+    const int units = d / 8;
+    const int threads = 128;
+    const dim3 grid(T, (units + threads - 1) / threads);
+    combine_kernel<<<grid, threads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d,
+                                                 static_cast<__nv_bfloat16 *>(y));
     return cudaGetLastError();
 }
 

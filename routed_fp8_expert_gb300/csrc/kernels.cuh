@@ -50,22 +50,26 @@ __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, in
 }
 
 // ------------------------------------------------------------------ top-k
-// One warp per token. Scores s = sigmoid(logit) in fp32; choice c = s + bias;
-// k rounds of a warp arg-max on (c desc, expert id asc); weights from s.
-__global__ void topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E,
-                            int k, float route_scale, int32_t *__restrict__ topk_idx,
+// One warp per token. The logit is the sum of the router GEMM's K-split
+// partials, added in split order; scores s = sigmoid(logit) in fp32; choice
+// c = s + bias; k rounds of a warp arg-max on (c desc, expert id asc); weights from s.
+__global__ void topk_kernel(const float *__restrict__ logits, int splits, const float *__restrict__ bias,
+                            int T, int E, int k, float route_scale, int32_t *__restrict__ topk_idx,
                             float *__restrict__ topk_w, float *__restrict__ scores) {
     const int lane = threadIdx.x & 31;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     const float *lrow = logits + static_cast<size_t>(t) * E;
+    const size_t split_stride = static_cast<size_t>(T) * E;
     float sv[32], cv[32];
     const int nper = (E + 31) >> 5;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int e = lane + 32 * i;
         if (i < nper && e < E) {
-            const float sc = 1.0f / (1.0f + expf(-lrow[e]));
+            float l = lrow[e];
+            for (int sp = 1; sp < splits; ++sp) l += lrow[sp * split_stride + e];
+            const float sc = 1.0f / (1.0f + expf(-l));
             sv[i] = sc;
             cv[i] = sc + bias[e];
             if (scores) scores[static_cast<size_t>(t) * E + e] = sc;
@@ -118,31 +122,36 @@ __global__ void topk_kernel(const float *__restrict__ logits, const float *__res
 // the ascending-token order inside every expert segment.
 constexpr int kPermWarps = 8;
 
-__global__ void perm_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int C,
+// One warp per chunk: a shared-memory word per expert collects the chunk's
+// lanes that chose it; ranks and counts are population counts of those words.
+// Ids outside [0, E) are skipped (rank -1), so bad input cannot write out of bounds.
+__global__ void perm_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int C,
                                  int32_t *__restrict__ rank, int32_t *__restrict__ cnt) {
-    extern __shared__ int32_t s_ids[];  // [kPermWarps][32 * k]
+    extern __shared__ uint32_t s_bits[];  // [kPermWarps][E]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x * kPermWarps + warp;
     if (c >= C) return;
-    int32_t *ids = s_ids + warp * 32 * k;
-    const int t = c * 32 + lane;
-    for (int j = 0; j < k; ++j) ids[lane * k + j] = (t < T) ? idx[static_cast<size_t>(t) * k + j] : -1;
+    uint32_t *bits = s_bits + warp * E;
+    for (int e = lane; e < E; e += 32) bits[e] = 0u;
     __syncwarp();
-    if (t >= T) return;
-    for (int j = 0; j < k; ++j) {
-        const int e = ids[lane * k + j];
-        int before = 0, after = 0;
-        for (int l = 0; l < 32; ++l) {
-            if (l == lane) continue;
-            for (int jj = 0; jj < k; ++jj) {
-                if (ids[l * k + jj] == e) {
-                    if (l < lane) ++before; else ++after;
-                }
-            }
+    const int t = c * 32 + lane;
+    const int32_t *row = idx + static_cast<size_t>(t) * k;
+    if (t < T) {
+        for (int j = 0; j < k; ++j) {
+            const int e = row[j];
+            if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicOr(&bits[e], 1u << lane);
         }
-        rank[static_cast<size_t>(t) * k + j] = before;
-        if (after == 0) cnt[static_cast<size_t>(e) * C + c] = before + 1;
     }
+    __syncwarp();
+    if (t < T) {
+        const uint32_t below = (1u << lane) - 1u;
+        for (int j = 0; j < k; ++j) {
+            const int e = row[j];
+            rank[static_cast<size_t>(t) * k + j] =
+                (static_cast<unsigned>(e) < static_cast<unsigned>(E)) ? __popc(bits[e] & below) : -1;
+        }
+    }
+    for (int e = lane; e < E; e += 32) cnt[static_cast<size_t>(e) * C + c] = __popc(bits[e]);
 }
 
 // Exclusive scan of one expert's per-chunk counts (in place); total -> counts[e].
@@ -227,32 +236,50 @@ __device__ void block_exclusive_scan(const int32_t *in, int n, int32_t *out, int
     __syncthreads();
 }
 
-// offsets[0..E] from counts[0..E-1]. Single block of 1024 threads (E <= 1024).
-__global__ void perm_offsets_kernel(const int32_t *__restrict__ counts, int E, int32_t *__restrict__ offsets) {
-    block_exclusive_scan<1>(counts, E, offsets, offsets + E);
-}
-
-// Segment table of the grouped GEMM: groups 0..E-1 are the routed experts'
-// segments (offsets), groups E..E+S-1 the shared experts' T rows each.
-//   row_start[g]   first activation row of group g; row_start[E+S] = (k+S)*T
-//   tile_prefix[g] prefix sum of ceil(rows_g / tile) over groups
-// Single block of 1024 threads (E + S <= 1028).
-__global__ void sched_kernel(const int32_t *__restrict__ offsets, int E, int S, int T, int k, int tile,
-                             int32_t *__restrict__ row_start, int32_t *__restrict__ tile_prefix) {
-    __shared__ int32_t s_tiles[2048];
+// Segment table of the grouped GEMMs from the routed offsets: groups 0..E-1
+// are the routed experts' segments, groups E..E+S-1 the shared experts' T rows.
+//   row_start[g]        first activation row of group g; row_start[E+S] = (k+S)*T
+//   tile_prefix_a/b[g]  prefix sums of ceil(rows_g / tile_a) and ceil(rows_g / tile_b)
+// (the gate/up and the down GEMM may use different token-tile widths), and the
+// two GEMMs' dynamic scheduler counters are reset to zero.
+// Called by a whole block of 1024 threads (E + S <= 1028).
+__device__ void schedule_block(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
+                               int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b,
+                               int32_t *counters) {
+    __shared__ int32_t s_rows[2048];
     const int G = E + S;
     const int kT = k * T;
-    for (int g = threadIdx.x; g <= G; g += blockDim.x) {
-        const int rs = (g <= E) ? offsets[g] : kT + (g - E) * T;
-        row_start[g] = rs;
-    }
+    if (threadIdx.x < 2) counters[threadIdx.x] = 0;   // the two GEMMs' dynamic scheduler counters
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) row_start[g] = (g <= E) ? offsets[g] : kT + (g - E) * T;
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
         const int a = (g < E) ? offsets[g] : kT + (g - E) * T;
         const int b = (g < E) ? offsets[g + 1] : kT + (g - E + 1) * T;
-        s_tiles[g] = (b - a + tile - 1) / tile;
+        s_rows[g] = (b - a + tile_a - 1) / tile_a;
     }
     __syncthreads();
-    block_exclusive_scan<2>(s_tiles, G, tile_prefix, tile_prefix + G);
+    block_exclusive_scan<2>(s_rows, G, tile_prefix_a, tile_prefix_a + G);
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const int a = (g < E) ? offsets[g] : kT + (g - E) * T;
+        const int b = (g < E) ? offsets[g + 1] : kT + (g - E + 1) * T;
+        s_rows[g] = (b - a + tile_b - 1) / tile_b;
+    }
+    __syncthreads();
+    block_exclusive_scan<2>(s_rows, G, tile_prefix_b, tile_prefix_b + G);
+}
+
+// offsets[0..E] from counts[0..E-1], then the GEMM schedules. Single block of 1024 threads.
+__global__ void perm_offsets_kernel(const int32_t *__restrict__ counts, int E, int S, int T, int k, int tile_a,
+                                    int tile_b, int32_t *__restrict__ offsets, int32_t *__restrict__ row_start,
+                                    int32_t *__restrict__ tile_prefix_a, int32_t *__restrict__ tile_prefix_b,
+                                    int32_t *__restrict__ counters) {
+    block_exclusive_scan<1>(counts, E, offsets, offsets + E);
+    schedule_block(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a, tile_prefix_b, counters);
+}
+
+__global__ void sched_kernel(const int32_t *__restrict__ offsets, int E, int S, int T, int k, int tile_a, int tile_b,
+                             int32_t *__restrict__ row_start, int32_t *__restrict__ tile_prefix_a,
+                             int32_t *__restrict__ tile_prefix_b, int32_t *__restrict__ counters) {
+    schedule_block(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a, tile_prefix_b, counters);
 }
 
 // One block per token: writes sorted_tok / inv_pos and copies the token's
@@ -261,7 +288,7 @@ __global__ void sched_kernel(const int32_t *__restrict__ offsets, int E, int S, 
 __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ rank,
                                     const int32_t *__restrict__ cnt_scan, const int32_t *__restrict__ offsets,
                                     const uint8_t *__restrict__ xq, const float *__restrict__ sx, int T, int k,
-                                    int S, int d, int C, int32_t *__restrict__ sorted_tok,
+                                    int S, int E, int d, int C, int32_t *__restrict__ sorted_tok,
                                     int32_t *__restrict__ inv_pos, uint8_t *__restrict__ xq_perm,
                                     float *__restrict__ sx_perm) {
     __shared__ int32_t s_pos[40];
@@ -272,10 +299,14 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
     if (threadIdx.x < k) {
         const int j = threadIdx.x;
         const int e = idx[static_cast<size_t>(t) * k + j];
-        const int pos = offsets[e] + cnt_scan[static_cast<size_t>(e) * C + c] + rank[static_cast<size_t>(t) * k + j];
+        int pos = -1;
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+            pos = offsets[e] + cnt_scan[static_cast<size_t>(e) * C + c] + rank[static_cast<size_t>(t) * k + j];
+            if (pos < 0 || pos >= k * T) pos = -1;
+        }
         s_pos[j] = pos;
         inv_pos[static_cast<size_t>(t) * k + j] = pos;
-        sorted_tok[pos] = t;
+        if (pos >= 0) sorted_tok[pos] = t;
     } else if (threadIdx.x < ndst) {
         s_pos[threadIdx.x] = k * T + (threadIdx.x - k) * T + t;
     }
@@ -285,17 +316,20 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
     for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
         const uint4 val = src[v];
         for (int j = 0; j < ndst; ++j)
-            reinterpret_cast<uint4 *>(xq_perm + static_cast<size_t>(s_pos[j]) * d)[v] = val;
+            if (s_pos[j] >= 0) reinterpret_cast<uint4 *>(xq_perm + static_cast<size_t>(s_pos[j]) * d)[v] = val;
     }
     const int gpr = d / 128;
     for (int g = threadIdx.x; g < gpr; g += blockDim.x) {
         const float sc = sx[static_cast<size_t>(t) * gpr + g];
-        for (int j = 0; j < ndst; ++j) sx_perm[static_cast<size_t>(g) * R + s_pos[j]] = sc;
+        for (int j = 0; j < ndst; ++j)
+            if (s_pos[j] >= 0) sx_perm[static_cast<size_t>(g) * R + s_pos[j]] = sc;
     }
 }
 
 // ------------------------------------------------------------------ combine
 // y[t] = sum_s o[kT + sT + t] + sum_j w[t, j] * o[inv_pos[t, j]] (fp32, fixed order) -> bf16.
+// Block (t, slice): blockDim.x threads, each owning 8 consecutive features of
+// the slice [slice * 8 * blockDim.x, ...) of token t.
 __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w,
                                const int32_t *__restrict__ inv_pos, int T, int k, int S, int d,
                                __nv_bfloat16 *__restrict__ y) {
@@ -307,36 +341,36 @@ __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float 
         s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
     }
     __syncthreads();
-    const int nvec = d / 8;
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-        float acc[8];
+    const int v = blockIdx.y * blockDim.x + threadIdx.x;   // 8-feature unit of token t
+    if (v >= d / 8) return;
+    float acc[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const uint4 raw = reinterpret_cast<const uint4 *>(o + (static_cast<size_t>(k) * T + static_cast<size_t>(s) * T + t) * d)[v];
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int s = 0; s < S; ++s) {
+        const uint4 raw = reinterpret_cast<const uint4 *>(o + (static_cast<size_t>(k) * T + static_cast<size_t>(s) * T + t) * d)[v];
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += __low2float(h[i]);
-                acc[2 * i + 1] += __high2float(h[i]);
-            }
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += __low2float(h[i]);
+            acc[2 * i + 1] += __high2float(h[i]);
         }
-        for (int j = 0; j < k; ++j) {
-            const uint4 raw = reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v];
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-            const float wj = s_w[j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(wj, __low2float(h[i]), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(wj, __high2float(h[i]), acc[2 * i + 1]);
-            }
-        }
-        uint4 out;
-        __nv_bfloat162 *oh = reinterpret_cast<__nv_bfloat162 *>(&out);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) oh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-        reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * d)[v] = out;
     }
+    for (int j = 0; j < k; ++j) {
+        if (s_pos[j] < 0) continue;
+        const uint4 raw = reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v];
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+        const float wj = s_w[j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wj, __low2float(h[i]), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wj, __high2float(h[i]), acc[2 * i + 1]);
+        }
+    }
+    uint4 out;
+    __nv_bfloat162 *oh = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) oh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * d)[v] = out;
 }
 
 }  // namespace moe
