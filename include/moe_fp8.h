@@ -107,6 +107,28 @@ int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx,
                 uint8_t *xq_perm, float *sx_perm,
                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* moe_permute without a caller workspace. The pages have no counterpart: this
+ * entry point exists for callers that cannot provide scratch memory, such as a
+ * plugin inside a host application that owns every device allocation, or a
+ * serving loop that may not call cudaMalloc after start-up (cudaMalloc
+ * synchronises the device and can fail when memory is tight).
+ * Arguments and outputs are those of moe_permute, minus the workspace. The
+ * scratch lives in one fixed device array inside the library (about 1.3 MB,
+ * held on every GPU that loads the library until the process exits), so:
+ *  - limits: T <= 8192 tokens, T * topk <= 65536 assignments, E <= 1024,
+ *    n_shared <= 4; larger calls return MOE_ERR_UNSUPPORTED and enqueue nothing;
+ *  - the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture;
+ *  - every call on a device shares the array: calls that may run at the same
+ *    time on the GPU (different streams without ordering) race and give wrong
+ *    results. Nothing in the array needs to be zero between calls;
+ *  - it allocates nothing and calls no allocating routine. */
+int moe_permute_noalloc(const int32_t *topk_idx, const uint8_t *xq, const float *sx,
+                        const moe_cfg_t *cfg, int T,
+                        int32_t *offsets, int32_t *sorted_tok, int32_t *inv_pos,
+                        uint8_t *xq_perm, float *sx_perm, void *stream);
+
 /* Grouped expert SwiGLU over FP8 weights ("Kimi-K2-Base", Feed-forward):
  * for each expert segment, o = down(silu(gate x) * up x), with h = silu(g) * u
  * quantised 1x128 between the two projections. Runs on the tcgen05 tensor

@@ -6,5 +6,5 @@ with ``routed_fp8_expert_gb300.build.build()``.
 """
 from ._lib import (MOE_ERR_ARG, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_OK,  # noqa: F401
                    MoeCfg, MoeError, cfg_of, check_device_error, combine, dense_swiglu_fp8, dense_workspace,
-                   expert_down_fp8, expert_gateup_fp8, expert_gemm_fp8, last_launch_count, layer_forward, load, permute, permuted_rows,
+                   expert_down_fp8, expert_gateup_fp8, expert_gemm_fp8, last_launch_count, layer_forward, load, permute, permute_noalloc, permuted_rows,
                    quant_fp8_1x128, route, workspace, workspace_bytes)

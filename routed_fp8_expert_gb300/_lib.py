@@ -33,6 +33,8 @@ _SIGS = {
     "moe_route": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_permute": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                              _c_size, _vp]),
+    "moe_permute_noalloc": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _vp,
+                                     _vp]),
     "moe_expert_gemm_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp,
                                      _c_size, _vp]),
     "moe_expert_gateup_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp,
@@ -150,6 +152,23 @@ def permute(topk_idx, xq, sx, cfg: MoeCfg, ws=None):
     ws = workspace(cfg, T, dev) if ws is None else ws
     _check(load().moe_permute(_p(topk_idx), _p(xq), _p(sx), ctypes.byref(cfg), T, _p(offsets), _p(sorted_tok),
                               _p(inv_pos), _p(xq_perm), _p(sx_perm), _p(ws), ws.numel(), _stream(dev)))
+    return offsets, sorted_tok, inv_pos, xq_perm, sx_perm
+
+
+def permute_noalloc(topk_idx, xq, sx, cfg: MoeCfg):
+    """moe_permute_noalloc: the permutation without a workspace (the library's
+    fixed device scratch; T <= 8192 and T * topk <= 65536). Outputs as permute()."""
+    _cuda(topk_idx, xq, sx)
+    T = topk_idx.shape[0]
+    dev = topk_idx.device
+    R = permuted_rows(cfg, T)
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    sorted_tok = torch.empty(T * cfg.topk, dtype=torch.int32, device=dev)
+    inv_pos = torch.empty((T, cfg.topk), dtype=torch.int32, device=dev)
+    xq_perm = torch.empty((R, cfg.d), dtype=torch.uint8, device=dev)
+    sx_perm = torch.empty((cfg.d // 128, R), dtype=torch.float32, device=dev)
+    _check(load().moe_permute_noalloc(_p(topk_idx), _p(xq), _p(sx), ctypes.byref(cfg), T, _p(offsets),
+                                      _p(sorted_tok), _p(inv_pos), _p(xq_perm), _p(sx_perm), _stream(dev)))
     return offsets, sorted_tok, inv_pos, xq_perm, sx_perm
 
 

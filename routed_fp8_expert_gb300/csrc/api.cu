@@ -313,6 +313,11 @@ int experts_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *of
 
 }  // namespace
 
+namespace moe {
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+void report_launches(int n) { t_launches = n; }
+}  // namespace moe
+
 extern "C" {
 
 int64_t moe_permuted_rows(const moe_cfg_t *cfg, int T) {

@@ -32,4 +32,9 @@ cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int
 cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos, int T, int k, int S, int d,
                            void *y, cudaStream_t stream);
 
+// Record the calling thread's last error text / launch count (api.cu), for
+// entry points defined in other translation units. report_error returns code.
+int report_error(int code, const char *msg);
+void report_launches(int n);
+
 }  // namespace moe
