@@ -86,18 +86,18 @@ int num_sms() {
 // Token-tile width of the expert GEMMs: expected rows per routed expert k*T/E
 // decides. Narrow tiles leave more shared memory to the weight pipeline; the
 // 64-token tile keeps every TMEM chunk of a K block in registers at once.
-int expert_bn(const moe_cfg_t &c, int T) {
-    const double rows = static_cast<double>(c.topk) * T / c.E;
-    return rows <= 12.0 ? 32 : 64;
-}
+//
+// Decode regime (<= 12 expected rows per expert): 32-token tiles and the fused
+// gate/up kernel, which streams the weights at the HBM rate. Beyond it:
+// 128-token tiles, with gate and up as separate items of the single-projection
+// kernel (one accumulator per column fits 128 columns in registers), followed
+// by the SwiGLU + quantise kernel. Wide tiles halve the MMA issues and the
+// weight bytes per token.
+bool decode_regime(const moe_cfg_t &c, int T) { return static_cast<double>(c.topk) * T / c.E <= 12.0; }
 
-// The down GEMM's epilogue holds one accumulator per column, so it can take
-// 128-token tiles beyond the decode regime (half the items and weight passes).
-int down_bn(const moe_cfg_t &c, int T) {
-    const double rows = static_cast<double>(c.topk) * T / c.E;
-    if (rows <= 12.0) return 32;
-    return rows <= 40.0 ? 64 : 128;
-}
+int expert_bn(const moe_cfg_t &c, int T) { return decode_regime(c, T) ? 32 : 128; }
+
+int down_bn(const moe_cfg_t &c, int T) { return decode_regime(c, T) ? 32 : 128; }
 
 int router_bn(int T) { return T <= 512 ? 32 : 128; }
 
@@ -141,6 +141,7 @@ struct LayerWs {
     uint8_t *hq;
     float *hs_t;
     __nv_bfloat16 *o;
+    float *gu;          // [2][R][H] fp32 gate and up projections (beyond the decode regime)
     size_t bytes;
 };
 
@@ -171,6 +172,7 @@ LayerWs carve_layer(const moe_cfg_t &c, int T, void *base) {
     w.hq = cv.take<uint8_t>(R * c.H);
     w.hs_t = cv.take<float>(R * (c.H / 128) * 4);
     w.o = cv.take<__nv_bfloat16>(R * c.d * 2);
+    w.gu = cv.take<float>(2 * R * c.H * 4);
     w.bytes = align_up(cv.off, 1024);
     return w;
 }
@@ -213,14 +215,21 @@ int make_map(CUtensorMap *m, const void *ptr, int elem_bytes, uint64_t rows, uin
     return MOE_OK;
 }
 
+// Activation maps with box heights 16, 32, 64 and 128 rows.
+int make_act_maps(ActMaps *m, const void *ptr, int elem_bytes, uint64_t rows, uint64_t cols) {
+    for (int i = 0; i < 4; ++i) MOE_CHECK(make_map(&m->box[i], ptr, elem_bytes, rows, cols, kActBoxRows << i));
+    return MOE_OK;
+}
+
 // ---------------------------------------------------------------- steps
 
 int route_impl(const void *x, const void *wg, const float *bias, const moe_cfg_t &c, int T, int32_t *idx,
                float *w, float *scores, float *logits, cudaStream_t st) {
     const int bn = router_bn(T);
-    CUtensorMap ma, mb;
+    CUtensorMap ma;
+    ActMaps mb;
     MOE_CHECK(make_map(&ma, wg, 2, c.E, c.d, kBM));
-    MOE_CHECK(make_map(&mb, x, 2, T, c.d, kActBoxRows));
+    MOE_CHECK(make_act_maps(&mb, x, 2, T, c.d));
     GemmArgs a{};
     a.G = 1;
     a.num_kb = c.d / 64;
@@ -249,9 +258,10 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
                  "schedule launch");
         t_launches += 1;
     }
-    CUtensorMap m13, mx;
+    CUtensorMap m13;
+    ActMaps mx;
     MOE_CHECK(make_map(&m13, w13, 1, static_cast<uint64_t>(G) * 2 * c.H, c.d, kBM));
-    MOE_CHECK(make_map(&mx, xq_perm, 1, R, c.d, kActBoxRows));
+    MOE_CHECK(make_act_maps(&mx, xq_perm, 1, R, c.d));
     GemmArgs gu{};
     gu.G = G;
     gu.num_kb = c.d / 128;
@@ -260,15 +270,25 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     gu.single_rows = -1;
     gu.row_start = ws.row_start;
     gu.tile_prefix = ws.tile_prefix;
-    gu.item_counter = ws.counters;
     gu.act_scale_t = sx_perm;
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * c.H;
     gu.a_second_offset = c.H;
-    gu.hq = hq;
-    gu.hs_t = hs;
-    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, bn, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
-    t_launches += 1;
+    if (decode_regime(c, T)) {
+        // fused gate/up + SiLU*mul + h quantisation; static item order (uniform
+        // items, one token tile per routed expert)
+        gu.hq = hq;
+        gu.hs_t = hs;
+        MOE_CUDA(launch_grouped_gemm(Kind::GateUp, bn, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
+        t_launches += 1;
+        return MOE_OK;
+    }
+    gu.n_proj = 2;
+    gu.out_f32 = ws.gu;
+    gu.item_counter = ws.counters;
+    MOE_CUDA(launch_grouped_gemm(Kind::Proj, bn, m13, mx, gu, num_sms(), st), "gate/up projection launch");
+    MOE_CUDA(launch_swiglu_quant(ws.gu, R, c.H, hq, hs, num_sms(), st), "SwiGLU quantise launch");
+    t_launches += 2;
     return MOE_OK;
 }
 
@@ -283,9 +303,10 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
                  "schedule launch");
         t_launches += 1;
     }
-    CUtensorMap m2, mh;
+    CUtensorMap m2;
+    ActMaps mh;
     MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, kBM));
-    MOE_CHECK(make_map(&mh, hq, 1, R, c.H, kActBoxRows));
+    MOE_CHECK(make_act_maps(&mh, hq, 1, R, c.H));
     GemmArgs dn{};
     dn.G = G;
     dn.num_kb = c.H / 128;
@@ -294,7 +315,7 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
     dn.single_rows = -1;
     dn.row_start = ws.row_start;
     dn.tile_prefix = ws.tile_prefix_dn;
-    dn.item_counter = ws.counters + 1;
+    dn.item_counter = decode_regime(c, T) ? nullptr : ws.counters + 1;
     dn.act_scale_t = hs;
     dn.w_scale = w2_s;
     dn.a_rows_per_group = c.d;
@@ -523,6 +544,7 @@ size_t dense_swiglu_workspace_bytes(int d, int H, int T) {
     cv.take<float>(Tz * (d / 128) * 4);
     cv.take<uint8_t>(Tz * H);
     cv.take<float>(Tz * (H / 128) * 4);
+    cv.take<float>(2 * Tz * H * 4);
     return align_up(cv.off, 1024);
 }
 
@@ -546,13 +568,15 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     float *sx_t = cv.take<float>(Tz * (d / 128) * 4);
     uint8_t *hq = cv.take<uint8_t>(Tz * H);
     float *hs_t = cv.take<float>(Tz * (H / 128) * 4);
+    float *gu_f32 = cv.take<float>(2 * Tz * H * 4);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     MOE_CUDA(launch_quant(x, true, T, d, xq, sx_t, true, num_sms(), st), "quantise launch");
-    CUtensorMap m13, mx, m2, mh;
+    CUtensorMap m13, m2;
+    ActMaps mx, mh;
     MOE_CHECK(make_map(&m13, w13, 1, static_cast<uint64_t>(2) * H, d, kBM));
-    MOE_CHECK(make_map(&mx, xq, 1, T, d, kActBoxRows));
+    MOE_CHECK(make_act_maps(&mx, xq, 1, T, d));
     MOE_CHECK(make_map(&m2, w2, 1, d, H, kBM));
-    MOE_CHECK(make_map(&mh, hq, 1, T, H, kActBoxRows));
+    MOE_CHECK(make_act_maps(&mh, hq, 1, T, H));
     GemmArgs gu{};
     gu.G = 1;
     gu.num_kb = d / 128;
@@ -563,9 +587,10 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * H;
     gu.a_second_offset = H;
-    gu.hq = hq;
-    gu.hs_t = hs_t;
-    MOE_CUDA(launch_grouped_gemm(Kind::GateUp, 64, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
+    gu.n_proj = 2;
+    gu.out_f32 = gu_f32;
+    MOE_CUDA(launch_grouped_gemm(Kind::Proj, 128, m13, mx, gu, num_sms(), st), "gate/up projection launch");
+    MOE_CUDA(launch_swiglu_quant(gu_f32, T, H, hq, hs_t, num_sms(), st), "SwiGLU quantise launch");
     GemmArgs dn{};
     dn.G = 1;
     dn.num_kb = H / 128;
@@ -577,7 +602,7 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     dn.a_rows_per_group = d;
     dn.out = static_cast<__nv_bfloat16 *>(y);
     MOE_CUDA(launch_grouped_gemm(Kind::Down, 128, m2, mh, dn, num_sms(), st), "down GEMM launch");
-    t_launches = 3;
+    t_launches = 4;
     return MOE_OK;
 }
 

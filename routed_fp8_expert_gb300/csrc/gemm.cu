@@ -11,7 +11,7 @@ cudaError_t device_error_word(unsigned int **ptr) {
 }
 
 template <Kind KIND, int BN>
-static cudaError_t launch_kind(const CUtensorMap &map_a, const CUtensorMap &map_b, const GemmArgs &args,
+static cudaError_t launch_kind(const CUtensorMap &map_a, const ActMaps &map_b, const GemmArgs &args,
                                int grid, cudaStream_t stream) {
     constexpr size_t smem = gemm_smem_bytes<KIND, BN>();
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -21,22 +21,28 @@ static cudaError_t launch_kind(const CUtensorMap &map_a, const CUtensorMap &map_
     return cudaGetLastError();
 }
 
-// Token-tile widths compiled per kind: the gate/up epilogue holds two
-// accumulators per column, so it stops at 64-token tiles.
+// Token-tile widths compiled per kind: the fused gate/up epilogue holds two
+// accumulators per column and serves the decode-sized tiles; the
+// single-projection kind serves the 128-token tiles.
 template <Kind KIND>
-static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const CUtensorMap &map_b, const GemmArgs &args,
+static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const ActMaps &map_b, const GemmArgs &args,
                              int grid, cudaStream_t stream) {
     switch (bn) {
-        case 32: return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
-        case 64: return launch_kind<KIND, 64>(map_a, map_b, args, grid, stream);
+        case 32:
+            if constexpr (KIND != Kind::Proj) return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
+            break;
+        case 64:
+            if constexpr (KIND != Kind::Proj) return launch_kind<KIND, 64>(map_a, map_b, args, grid, stream);
+            break;
         case 128:
             if constexpr (KIND != Kind::GateUp) return launch_kind<KIND, 128>(map_a, map_b, args, grid, stream);
             break;
+        default: break;
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, const CUtensorMap &map_b,
+cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, const ActMaps &map_b,
                                 GemmArgs &args, int grid, cudaStream_t stream) {
     cudaError_t e = device_error_word(&args.err);
     if (e != cudaSuccess) return e;
@@ -44,6 +50,7 @@ cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, con
         case Kind::GateUp: return launch_bn<Kind::GateUp>(bn, map_a, map_b, args, grid, stream);
         case Kind::Down: return launch_bn<Kind::Down>(bn, map_a, map_b, args, grid, stream);
         case Kind::Router: return launch_bn<Kind::Router>(bn, map_a, map_b, args, grid, stream);
+        case Kind::Proj: return launch_bn<Kind::Proj>(bn, map_a, map_b, args, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -11,8 +11,9 @@
 //               TMA tile loads (weight tile(s) + activation rows per 128-byte K
 //               block) and copies the scales of each stage
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..   epilogue: 2 or 4 column groups of four warps; each warp reads
-//               its 32-lane quarter of TMEM for its group's token columns
+//   warps 2..9  epilogue: 2 column groups of four warps; each warp reads its
+//               32-lane quarter of TMEM for its group's token columns
+//   last warp   (FP8 kinds) copies each K block's activation and weight scales
 //
 // Tile scheduler: for expert groups the producer takes the next item from a
 // global counter (atomicAdd), so token tiles that share a weight block start
@@ -32,16 +33,23 @@
 // Router kind: bf16 x bf16 -> fp32, accumulated in TMEM over the whole K
 // range; the epilogue writes fp32 logits.
 #pragma once
+#include "internal.h"
 #include "ptx.cuh"
 
 namespace moe {
 
-enum class Kind { GateUp, Down, Router };
+// GateUp: gate and up projections of one weight block, fused SiLU*mul and h quantisation.
+// Proj:   one projection (gate or up) per item, fp32 output; SiLU*mul and h
+//         quantisation follow in a separate kernel. Items carry half the weight
+//         tiles of GateUp, so 128-token tiles fit the epilogue's registers.
+// Down:   down projection, bf16 output.
+// Router: bf16 router logits.
+enum class Kind { GateUp, Down, Router, Proj };
 
 constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
 constexpr int kATileBytes = kBM * kKBytes;  // 16 KB
-constexpr int kActBoxRows = 16;             // activation TMA box height
+constexpr int kActBoxRows = 16;             // smallest activation TMA box height
 constexpr int kMaxGroups = 1032;            // routed + shared experts, padded
 constexpr int kItemQ = 4;                   // depth of the producer -> consumers item queue
 
@@ -65,11 +73,12 @@ template <Kind K, int BN> struct KindCfg {
     // scale slots: their own ring, released by the epilogue, so operand stages
     // are released by the MMA alone and the producer keeps kStages ahead of it
     static constexpr int kScaleSlots = kPromote ? (kStages + kNumPart + 2) : 1;
-    static constexpr int kGroups = 2;                             // epilogue column groups
+    static constexpr int kGroups = 2;                              // epilogue column groups
     static constexpr int kHalfCols = BN / kGroups;                // token columns per column group
     static constexpr int kChunks = kHalfCols / 16;
     static constexpr int kEpiWarps = 4 * kGroups;                 // one warp per TMEM lane quarter and group
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kScaleWarp = 2 + kEpiWarps;               // copies the K blocks' scales
+    static constexpr int kThreads = 64 + 32 * kEpiWarps + (kPromote ? 32 : 0);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
     static_assert(kStages >= 3, "pipeline depth");
 };
@@ -89,6 +98,8 @@ struct GemmArgs {
     uint8_t *hq;              // GateUp: [total_rows][num_mb*128]
     float *hs_t;              // GateUp: [num_mb][total_rows]
     __nv_bfloat16 *out;       // Down: [total_rows][num_mb*128]
+    float *out_f32;           // Proj: [2][total_rows][num_mb*128] gate (0) and up (1) projections
+    int n_proj;               // Proj: 2 (items per weight block: gate, up); 1 otherwise
     float *logits;            // Router: [k_splits][total_rows][n_valid] partial logits
     int n_valid;              // Router: valid weight rows (experts)
     int k_splits;             // Router: K range split into this many partial sums (>= 1)
@@ -98,51 +109,60 @@ struct GemmArgs {
 
 struct Item {
     int g, mb, row0, n, ks;
+    int proj;     // Proj: 0 gate, 1 up
     int ntiles;   // token tiles of the item's group (tiles sharing its weight block)
 };
 
+// Items of a group are ordered (weight block, projection, token tile) with the
+// token tile fastest, so the tiles that share a weight block are adjacent.
 template <int BN>
 __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int *s_tp,
                                             const int *s_rs, Item &o) {
+    const int nproj = a.n_proj > 1 ? a.n_proj : 1;
+    const int nblk = a.num_mb * nproj;   // weight blocks x projections
+    int mbx;
     if (a.single_rows >= 0) {
-        // items = (mb, token tile, K split) with the split fastest
+        // items = (block, token tile, K split) with the split fastest
         const int nt_total = (a.single_rows + BN - 1) / BN;
         const int splits = a.k_splits > 0 ? a.k_splits : 1;
         o.ks = it % splits;
         const int rest = it / splits;
         o.g = 0;
-        o.mb = rest / nt_total;
-        const int nt = rest - o.mb * nt_total;
+        mbx = rest / nt_total;
+        const int nt = rest - mbx * nt_total;
         o.row0 = nt * BN;
         o.n = min(BN, a.single_rows - o.row0);
         o.ntiles = nt_total;
-        return o.n > 0 && o.mb < a.num_mb;
+    } else {
+        o.ks = 0;
+        const int key = it / nblk;
+        int lo = 0, hi = a.G;  // find the last g with tile_prefix[g] <= key
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_tp[mid] <= key) lo = mid; else hi = mid;
+        }
+        const int g = lo;
+        const int nt_g = s_tp[g + 1] - s_tp[g];
+        if (nt_g <= 0) return false;
+        const int li = it - nblk * s_tp[g];
+        o.g = g;
+        mbx = li / nt_g;
+        const int nt = li - mbx * nt_g;
+        o.row0 = s_rs[g] + nt * BN;
+        o.n = min(BN, s_rs[g + 1] - o.row0);
+        o.ntiles = nt_g;
     }
-    o.ks = 0;
-    const int key = it / a.num_mb;
-    int lo = 0, hi = a.G;  // find the last g with tile_prefix[g] <= key
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_tp[mid] <= key) lo = mid; else hi = mid;
-    }
-    const int g = lo;
-    const int nt_g = s_tp[g + 1] - s_tp[g];
-    if (nt_g <= 0) return false;
-    const int li = it - a.num_mb * s_tp[g];
-    o.g = g;
-    o.mb = li / nt_g;
-    const int nt = li - o.mb * nt_g;
-    o.row0 = s_rs[g] + nt * BN;
-    o.n = min(BN, s_rs[g + 1] - o.row0);
-    o.ntiles = nt_g;
+    o.mb = mbx / nproj;
+    o.proj = mbx - o.mb * nproj;
     return o.n > 0 && o.mb < a.num_mb;
 }
 
 template <int BN>
 __device__ __forceinline__ int total_items(const GemmArgs &a, const int *s_tp) {
+    const int nblk = a.num_mb * (a.n_proj > 1 ? a.n_proj : 1);
     if (a.single_rows >= 0)
-        return a.num_mb * ((a.single_rows + BN - 1) / BN) * (a.k_splits > 0 ? a.k_splits : 1);
-    return a.num_mb * s_tp[a.G];
+        return nblk * ((a.single_rows + BN - 1) / BN) * (a.k_splits > 0 ? a.k_splits : 1);
+    return nblk * s_tp[a.G];
 }
 
 // K blocks [kb0, kb1) of one item.
@@ -176,7 +196,7 @@ template <Kind KIND, int BN> struct SmemLayout {
 
 template <Kind KIND, int BN>
 __global__ void __launch_bounds__(KindCfg<KIND, BN>::kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ ActMaps map_b,
                     const GemmArgs args) {
     using C = KindCfg<KIND, BN>;
     using L = SmemLayout<KIND, BN>;
@@ -224,7 +244,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             mbar_init(smem_u32(&empty[s]), 1);   // the MMA commit
         }
         for (int s = 0; s < C::kScaleSlots; ++s) {
-            mbar_init(smem_u32(&sfull[s]), 32);    // one cp.async arrival per producer lane
+            mbar_init(smem_u32(&sfull[s]), 32);    // one cp.async arrival per scale-warp lane
             mbar_init(smem_u32(&sempty[s]), kEpi); // one arrival per epilogue warp
         }
         for (int b = 0; b < C::kNumPart; ++b) {
@@ -235,12 +255,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         for (int b = 0; b < 2 * C::kGroups; ++b) mbar_init(smem_u32(&amax_bar[b]), 4);
         for (int b = 0; b < kItemQ; ++b) {
             mbar_init(smem_u32(&item_full[b]), 1);
-            mbar_init(smem_u32(&item_empty[b]), 1 + kEpi);
+            mbar_init(smem_u32(&item_empty[b]), 1 + kEpi + (C::kPromote ? 1 : 0));
         }
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&map_a);
-        tma_prefetch_desc(&map_b);
+        for (int i = 0; i < 4; ++i) tma_prefetch_desc(&map_b.box[i]);
     }
     if (warp == 1) tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
     tc_fence_before();
@@ -261,8 +281,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // lane 0 fetches items and issues the TMA tile loads; all lanes copy the
-        // stage's scales (activation scales of the tile's tokens, weight scales)
+        // lane 0 fetches items and issues the TMA tile loads
         // weights read by one token tile only are streamed (evict first); a weight
         // block shared by several token tiles, which run at the same time, stays
         // in L2 for them (normal policy)
@@ -271,8 +290,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         const uint64_t pol_x = policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
-        int sslot = 0;
-        uint32_t sphase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
         int q = 0;
         uint32_t qphase = 0;
@@ -300,31 +317,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             }
             int kb0, kb1;
             kb_range(args, I, kb0, kb1);
-            const int nb16 = (I.n + kActBoxRows - 1) / kActBoxRows;
-            const uint32_t bytes = C::kATiles * kATileBytes + nb16 * kActBoxRows * kKBytes;
+            // one activation box: the smallest of 16/32/64/128 rows that covers the tile
+            const int box_i = (I.n <= 16) ? 0 : (I.n <= 32) ? 1 : (I.n <= 64) ? 2 : 3;
+            const uint32_t bytes = C::kATiles * kATileBytes + (kActBoxRows << box_i) * kKBytes;
             const uint64_t pol_w = (I.ntiles > 1) ? pol_shared : pol_stream;
             int arow0, arow1 = 0;
-            const float *ws0 = nullptr, *ws1 = nullptr;
             if constexpr (KIND == Kind::Router) {
                 arow0 = I.mb * kBM;
             } else {
                 arow0 = I.g * args.a_rows_per_group + I.mb * kBM;
                 arow1 = arow0 + args.a_second_offset;
-                if constexpr (KIND == Kind::GateUp) {
-                    ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
-                    ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
-                } else {
-                    ws0 = args.w_scale + (static_cast<size_t>(I.g) * args.num_mb + I.mb) * args.num_kb;
-                }
+                if constexpr (KIND == Kind::Proj) arow0 += I.proj * args.a_second_offset;
             }
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
                 int w = 1;
-                if (lane == 0) {
-                    w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
-                    if (C::kPromote && w)
-                        w = mbar_wait(smem_u32(&sempty[sslot]), sphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
-                }
+                if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w) { ok = false; break; }
                 const uint32_t fb = smem_u32(&full[stage]);
@@ -334,20 +342,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const int kx = kb * kKbElems;
                     tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
                     if constexpr (C::kATiles == 2) tma_load_2d(sbase + kATileBytes, &map_a, fb, kx, arow1, pol_w);
-                    const uint32_t bdst = sbase + C::kATiles * kATileBytes;
-                    for (int i = 0; i < nb16; ++i)
-                        tma_load_2d(bdst + i * kActBoxRows * kKBytes, &map_b, fb, kx, I.row0 + i * kActBoxRows, pol_x);
-                }
-                if constexpr (C::kPromote) {
-                    const uint32_t sdst = smem_u32(s_scale + sslot * L::kScaleStride);
-                    const float *src = args.act_scale_t + static_cast<size_t>(kb) * args.total_rows + I.row0;
-                    for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
-                    if (lane == 0) {
-                        cp_async_4(sdst + 4 * BN, ws0 + kb);
-                        if constexpr (KIND == Kind::GateUp) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
-                    }
-                    cp_async_arrive_noinc(smem_u32(&sfull[sslot]));
-                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
+                    tma_load_2d(sbase + C::kATiles * kATileBytes, &map_b.box[box_i], fb, kx, I.row0, pol_x);
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -356,7 +351,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             if (!ok) break;
         }
         // every issued copy must land before the CTA may exit
-        if constexpr (C::kPromote) cp_async_wait_all();
         if (lane == 0)
             for (int s = 0; s < C::kStages; ++s)
                 if (issued_mask & (1u << s)) mbar_wait_drain(smem_u32(&full[s]), (issued_parity >> s) & 1u, args.err);
@@ -413,7 +407,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             mma_commit(smem_u32(mma_done));
             mbar_wait_drain(smem_u32(mma_done), 0, args.err);
         }
-    } else {
+    } else if (C::kPromote && warp == C::kScaleWarp) {
+        // ------------------------------------------------------------ scale copier
+        // per K block: the activation scales of the tile's tokens and the weight
+        // scale(s) of the block, into the next scale slot (cp.async, 4 bytes per
+        // lane and copy); runs beside the producer so the TMA issue never waits
+        // on these copies
+        int sslot = 0;
+        uint32_t sphase = 0;
+        int q = 0;
+        uint32_t qphase = 0;
+        bool ok = true;
+        while (ok) {
+            int it = 0;
+            if (lane == 0) it = take_item(q, qphase);
+            it = __shfl_sync(0xffffffffu, it, 0);
+            if (it < 0 || it >= n_items) break;
+            Item I;
+            if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
+            const float *ws0, *ws1 = nullptr;
+            if constexpr (KIND == Kind::Proj) {
+                ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + I.proj) * args.num_mb + I.mb) * args.num_kb;
+            } else if constexpr (KIND == Kind::GateUp) {
+                ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
+                ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
+            } else {
+                ws0 = args.w_scale + (static_cast<size_t>(I.g) * args.num_mb + I.mb) * args.num_kb;
+            }
+            for (int kb = 0; kb < args.num_kb; ++kb) {
+                int w = 1;
+                if (lane == 0) w = mbar_wait(smem_u32(&sempty[sslot]), sphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) { ok = false; break; }
+                const uint32_t sdst = smem_u32(s_scale + sslot * L::kScaleStride);
+                const float *src = args.act_scale_t + static_cast<size_t>(kb) * args.total_rows + I.row0;
+                for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
+                if (lane == 0) {
+                    cp_async_4(sdst + 4 * BN, ws0 + kb);
+                    if constexpr (KIND == Kind::GateUp) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
+                }
+                cp_async_arrive_noinc(smem_u32(&sfull[sslot]));
+                if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
+            }
+        }
+        cp_async_wait_all();   // the copies must land before the CTA may exit
+    } else if (warp >= 2 && warp < 2 + kEpi) {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;
         const int quad = warp & 3;           // TMEM lane quarter this warp may access
@@ -533,6 +571,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                             const size_t row = static_cast<size_t>(I.row0 + col_base + j);
                             args.hq[row * H + I.mb * kBM + wrow] = code;
                             if (wrow == 0) args.hs_t[static_cast<size_t>(I.mb) * args.total_rows + row] = s;
+                        }
+                    }
+                } else if constexpr (KIND == Kind::Proj) {
+                    const int H = args.num_mb * kBM;
+                    float *dst = args.out_f32 + static_cast<size_t>(I.proj) * args.total_rows * H;
+#pragma unroll
+                    for (int j = 0; j < HC; ++j) {
+                        if (j < n_my) {
+                            const size_t row = static_cast<size_t>(I.row0 + col_base + j);
+                            dst[row * H + I.mb * kBM + wrow] = acc0[j];
                         }
                     }
                 } else {

@@ -9,8 +9,15 @@ namespace moe {
 struct GemmArgs;
 enum class Kind;
 
+// Tensor maps of one activation matrix with box heights 16, 32, 64 and 128 rows
+// (128 bytes wide, 128-byte swizzle): a token tile is loaded with the smallest
+// single box that covers its rows.
+struct ActMaps {
+    CUtensorMap box[4];
+};
+
 // Grouped tcgen05 GEMM launch (gemm.cu). Returns a cudaError_t.
-cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, const CUtensorMap &map_b,
+cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, const ActMaps &map_b,
                                 GemmArgs &args, int grid, cudaStream_t stream);
 // Address of the device error word on the current device (gemm.cu).
 cudaError_t device_error_word(unsigned int **ptr);
@@ -18,6 +25,8 @@ cudaError_t device_error_word(unsigned int **ptr);
 // Small kernels (kernels.cu).
 cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint8_t *q, float *s,
                          bool s_transposed, int num_sms, cudaStream_t stream);
+cudaError_t launch_swiglu_quant(const float *gu, int64_t rows, int H, uint8_t *hq, float *hs, int num_sms,
+                                cudaStream_t stream);
 cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream);
 cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *sx, int T, int k, int S, int E,
