@@ -53,10 +53,13 @@ WORKLOADS = {"decode": S.DECODE, "prefill": S.PREFILL, "skewed": S.SKEWED, "dens
 DATA = ("synthetic, seeded: x ~ N(0,1) bf16; W_g ~ N(0,0.02) bf16; bias ~ N(0,0.01) fp32 (+0.5 on 16 hot "
         "experts for the skewed workload); expert weights ~ N(0,0.02) stored e4m3 with 128x128 fp32 scales")
 
-# dram bytes (read + write) per launch of the gate/up kernel from one ncu capture,
-# keyed by the hash of the kernel sources at capture time: when the sources
-# change, the figure no longer applies and is reported as null.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the decode gate/up kernel, from one ncu
+# capture of the same kernel on the decode-like case of a few GB (decode_e64:
+# 1.9157 GB of traffic for 1.9130 GB of algorithmic bytes). Traffic grows with
+# the touched experts' weights, so the full launch's figure is this ratio times
+# its algorithmic bytes. Keyed by the hash of the kernel sources at capture
+# time: once the sources change, the figure no longer applies (null).
+NCU_TRAFFIC = {"ratio": 1.0014, "src": "9e188652a31b5efd", "case": "decode_e64"}
 
 
 def kernel_src_hash() -> str:
@@ -65,6 +68,11 @@ def kernel_src_hash() -> str:
         with open(os.path.join(ROOT, "routed_fp8_expert_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def expert_bn_is_decode(shape) -> bool:
+    """The decode regime (fused gate/up kernel, 32-token tiles) that the capture covers."""
+    return shape.topk * shape.T / shape.E <= 12.0
 
 
 def measured_peaks() -> dict:
@@ -367,8 +375,9 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
                 + R * d + R * (d // 128) * 4 + R * H + R * (H // 128) * 4)
     gu_ms = per["gateup"]
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC.get(shape.name)
-    traffic_val = traffic["bytes"] if traffic and traffic.get("src") == kernel_src_hash() else None
+    traffic_val = None
+    if NCU_TRAFFIC and NCU_TRAFFIC.get("src") == kernel_src_hash() and expert_bn_is_decode(shape):
+        traffic_val = NCU_TRAFFIC["ratio"] * gu_bytes
     layer_weight_bytes = touched * (3 * H * d + 3 * (H // 128) * (d // 128) * 4) + E * d * 2
     flops = T * (2 * E * d) + (T * k + T * Sh) * 6 * d * H
     ms_step = ms_total / args.steps
@@ -406,7 +415,9 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3", "data": DATA, "config": workload_config(shape),
-        "roofline": {"bound": "hbm", "kernel": "grouped_gemm_kernel<GateUp>", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": ("grouped_gemm_kernel<GateUp, 32>" if expert_bn_is_decode(shape) else
+                                                 "grouped_gemm_kernel<Proj, 128> + swiglu_quant_kernel"),
+                     "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic_val, "alg_bytes_per_launch": gu_bytes,
                      "launch_ms": gu_ms, "peak_source": peaks["source"] + " (MEASURED_PEAKS hbm_gbs copy bandwidth)"},

@@ -320,7 +320,14 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
     dn.w_scale = w2_s;
     dn.a_rows_per_group = c.d;
     dn.out = static_cast<__nv_bfloat16 *>(o);
-    MOE_CUDA(launch_grouped_gemm(Kind::Down, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    if (decode_regime(c, T) && (c.d / 128) % 2 == 0) {
+        // decode: two adjacent 128-row blocks per item (32 KB of weights per K block)
+        dn.num_mb = c.d / 256;
+        dn.a_second_offset = kBM;
+        MOE_CUDA(launch_grouped_gemm(Kind::DownPair, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    } else {
+        MOE_CUDA(launch_grouped_gemm(Kind::Down, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    }
     t_launches += 1;
     return MOE_OK;
 }

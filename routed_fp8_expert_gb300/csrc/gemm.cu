@@ -32,10 +32,12 @@ static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const ActMaps &ma
             if constexpr (KIND != Kind::Proj) return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
             break;
         case 64:
-            if constexpr (KIND != Kind::Proj) return launch_kind<KIND, 64>(map_a, map_b, args, grid, stream);
+            if constexpr (KIND != Kind::Proj && KIND != Kind::DownPair)
+                return launch_kind<KIND, 64>(map_a, map_b, args, grid, stream);
             break;
         case 128:
-            if constexpr (KIND != Kind::GateUp) return launch_kind<KIND, 128>(map_a, map_b, args, grid, stream);
+            if constexpr (KIND != Kind::GateUp && KIND != Kind::DownPair)
+                return launch_kind<KIND, 128>(map_a, map_b, args, grid, stream);
             break;
         default: break;
     }
@@ -51,6 +53,7 @@ cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, con
         case Kind::Down: return launch_bn<Kind::Down>(bn, map_a, map_b, args, grid, stream);
         case Kind::Router: return launch_bn<Kind::Router>(bn, map_a, map_b, args, grid, stream);
         case Kind::Proj: return launch_bn<Kind::Proj>(bn, map_a, map_b, args, grid, stream);
+        case Kind::DownPair: return launch_bn<Kind::DownPair>(bn, map_a, map_b, args, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -43,8 +43,11 @@ namespace moe {
 //         quantisation follow in a separate kernel. Items carry half the weight
 //         tiles of GateUp, so 128-token tiles fit the epilogue's registers.
 // Down:   down projection, bf16 output.
+// DownPair: down projection with two adjacent 128-row weight blocks per item
+//         (like GateUp's two tiles): twice the weight bytes per K block for the
+//         same per-K-block fixed costs; used for decode-sized tiles.
 // Router: bf16 router logits.
-enum class Kind { GateUp, Down, Router, Proj };
+enum class Kind { GateUp, Down, Router, Proj, DownPair };
 
 constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
@@ -59,7 +62,8 @@ constexpr int pow2_at_least(int v, int lo) { return v <= lo ? lo : 2 * pow2_at_l
 
 // Per-kind, per-tile-width configuration. BN = tokens per tile (MMA N upper bound).
 template <Kind K, int BN> struct KindCfg {
-    static constexpr int kATiles = (K == Kind::GateUp) ? 2 : 1;   // gate and up weight tiles
+    // weight tiles per K block: gate and up (GateUp) or two row blocks (DownPair)
+    static constexpr int kATiles = (K == Kind::GateUp || K == Kind::DownPair) ? 2 : 1;
     static constexpr bool kPromote = (K != Kind::Router);         // per-128-K fp32 promotion
     static constexpr bool kBf16 = (K == Kind::Router);
     static constexpr int kBTileBytes = BN * kKBytes;
@@ -325,7 +329,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             if constexpr (KIND == Kind::Router) {
                 arow0 = I.mb * kBM;
             } else {
-                arow0 = I.g * args.a_rows_per_group + I.mb * kBM;
+                constexpr int kRowsPerBlock = (KIND == Kind::DownPair) ? 2 * kBM : kBM;
+                arow0 = I.g * args.a_rows_per_group + I.mb * kRowsPerBlock;
                 arow1 = arow0 + args.a_second_offset;
                 if constexpr (KIND == Kind::Proj) arow0 += I.proj * args.a_second_offset;
             }
@@ -431,6 +436,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             } else if constexpr (KIND == Kind::GateUp) {
                 ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
                 ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
+            } else if constexpr (KIND == Kind::DownPair) {
+                // row blocks 2mb and 2mb+1 of the group's [2 * num_mb][num_kb] scale grid
+                ws0 = args.w_scale + (static_cast<size_t>(I.g) * 2 * args.num_mb + 2 * I.mb) * args.num_kb;
+                ws1 = ws0 + args.num_kb;
             } else {
                 ws0 = args.w_scale + (static_cast<size_t>(I.g) * args.num_mb + I.mb) * args.num_kb;
             }
@@ -444,7 +453,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
                 if (lane == 0) {
                     cp_async_4(sdst + 4 * BN, ws0 + kb);
-                    if constexpr (KIND == Kind::GateUp) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
+                    if constexpr (C::kATiles == 2) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
                 }
                 cp_async_arrive_noinc(smem_u32(&sfull[sslot]));
                 if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
@@ -475,7 +484,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
             const int n_my = max(0, min(HC, I.n - col_base));
             if constexpr (C::kPromote) {
-                constexpr bool kTwo = (KIND == Kind::GateUp);
+                constexpr bool kTwo = (C::kATiles == 2);
                 float acc0[HC], acc1[HC];
 #pragma unroll
                 for (int j = 0; j < HC; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
@@ -581,6 +590,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                         if (j < n_my) {
                             const size_t row = static_cast<size_t>(I.row0 + col_base + j);
                             dst[row * H + I.mb * kBM + wrow] = acc0[j];
+                        }
+                    }
+                } else if constexpr (KIND == Kind::DownPair) {
+                    const int dout = args.num_mb * 2 * kBM;
+#pragma unroll
+                    for (int j = 0; j < HC; ++j) {
+                        if (j < n_my) {
+                            const size_t row = static_cast<size_t>(I.row0 + col_base + j);
+                            __nv_bfloat16 *o = args.out + row * dout + I.mb * 2 * kBM + wrow;
+                            o[0] = __float2bfloat16_rn(acc0[j]);
+                            o[kBM] = __float2bfloat16_rn(acc1[j]);
                         }
                     }
                 } else {

@@ -31,8 +31,8 @@ cudaError_t launch_swiglu_quant(const float *gu, int64_t rows, int H, uint8_t *h
 
 cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream) {
-    const int threads = 256;  // 8 tokens per block
-    topk_kernel<<<(T + 7) / 8, threads, 0, stream>>>(logits, splits, bias, T, E, k, scale, idx, w, scores);
+    const int threads = 64;   // 2 tokens per block: a 256-token batch spreads over 128 blocks
+    topk_kernel<<<(T + 1) / 2, threads, 0, stream>>>(logits, splits, bias, T, E, k, scale, idx, w, scores);
     return cudaGetLastError();
 }
 

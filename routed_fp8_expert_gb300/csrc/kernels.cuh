@@ -96,13 +96,20 @@ __global__ void topk_kernel(const float *__restrict__ logits, int splits, const 
     const size_t split_stride = static_cast<size_t>(T) * E;
     float sv[32], cv[32];
     const int nper = (E + 31) >> 5;
+    // logits: the split partials added in split order (independent loads per split)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sv[i] = (i < nper && lane + 32 * i < E) ? lrow[lane + 32 * i] : 0.f;
+    for (int sp = 1; sp < splits; ++sp) {
+        const float *prow = lrow + sp * split_stride;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nper && lane + 32 * i < E) sv[i] += prow[lane + 32 * i];
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int e = lane + 32 * i;
         if (i < nper && e < E) {
-            float l = lrow[e];
-            for (int sp = 1; sp < splits; ++sp) l += lrow[sp * split_stride + e];
-            const float sc = 1.0f / (1.0f + expf(-l));
+            const float sc = 1.0f / (1.0f + expf(-sv[i]));
             sv[i] = sc;
             cv[i] = sc + bias[e];
             if (scores) scores[static_cast<size_t>(t) * E + e] = sc;
