@@ -215,6 +215,23 @@ int make_map(CUtensorMap *m, const void *ptr, int elem_bytes, uint64_t rows, uin
     return MOE_OK;
 }
 
+// The gate/up weights [G][2][H][d] as a 3D map (x = d, y = H, z = 2G) whose box
+// {128 bytes, 128 rows, 2} holds one row block of gate_proj and the same rows of
+// up_proj: one request per K block.
+int make_map_gateup(CUtensorMap *m, const void *ptr, uint64_t G, uint64_t H, uint64_t d) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[3] = {d, H, 2 * G};
+    cuuint64_t strides[2] = {d, H * d};
+    cuuint32_t box[3] = {128, 128, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (3D) failed (%d)", static_cast<int>(r));
+    return MOE_OK;
+}
+
 // Activation maps with box heights 16, 32, 64 and 128 rows.
 int make_act_maps(ActMaps *m, const void *ptr, int elem_bytes, uint64_t rows, uint64_t cols) {
     for (int i = 0; i < 4; ++i) MOE_CHECK(make_map(&m->box[i], ptr, elem_bytes, rows, cols, kActBoxRows << i));
@@ -277,6 +294,7 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     if (decode_regime(c, T)) {
         // fused gate/up + SiLU*mul + h quantisation; static item order (uniform
         // items, one token tile per routed expert)
+        MOE_CHECK(make_map_gateup(&m13, w13, G, c.H, c.d));
         gu.hq = hq;
         gu.hs_t = hs;
         MOE_CUDA(launch_grouped_gemm(Kind::GateUp, bn, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
@@ -321,7 +339,9 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
     dn.a_rows_per_group = c.d;
     dn.out = static_cast<__nv_bfloat16 *>(o);
     if (decode_regime(c, T) && (c.d / 128) % 2 == 0) {
-        // decode: two adjacent 128-row blocks per item (32 KB of weights per K block)
+        // decode: two adjacent 128-row blocks per item, one 256-row box (32 KB of
+        // weights per K block and request)
+        MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
         dn.num_mb = c.d / 256;
         dn.a_second_offset = kBM;
         MOE_CUDA(launch_grouped_gemm(Kind::DownPair, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");

@@ -325,13 +325,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             const int box_i = (I.n <= 16) ? 0 : (I.n <= 32) ? 1 : (I.n <= 64) ? 2 : 3;
             const uint32_t bytes = C::kATiles * kATileBytes + (kActBoxRows << box_i) * kKBytes;
             const uint64_t pol_w = (I.ntiles > 1) ? pol_shared : pol_stream;
-            int arow0, arow1 = 0;
+            int arow0;
             if constexpr (KIND == Kind::Router) {
                 arow0 = I.mb * kBM;
             } else {
                 constexpr int kRowsPerBlock = (KIND == Kind::DownPair) ? 2 * kBM : kBM;
                 arow0 = I.g * args.a_rows_per_group + I.mb * kRowsPerBlock;
-                arow1 = arow0 + args.a_second_offset;
                 if constexpr (KIND == Kind::Proj) arow0 += I.proj * args.a_second_offset;
             }
             bool ok = true;
@@ -345,8 +344,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, bytes);
                     const int kx = kb * kKbElems;
-                    tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
-                    if constexpr (C::kATiles == 2) tma_load_2d(sbase + kATileBytes, &map_a, fb, kx, arow1, pol_w);
+                    // weight tiles in one request (the TMA unit's request rate, not its
+                    // bytes, bounds an SM's loads): GateUp's gate and up tiles as one
+                    // 3D box, DownPair's two row blocks as one 256-row box
+                    if constexpr (KIND == Kind::GateUp)
+                        tma_load_3d(sbase, &map_a, fb, kx, I.mb * kBM, 2 * I.g, pol_w);
+                    else
+                        tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
                     tma_load_2d(sbase + C::kATiles * kATileBytes, &map_b.box[box_i], fb, kx, I.row0, pol_x);
                 }
                 issued_mask |= 1u << stage;
