@@ -95,9 +95,16 @@ int num_sms() {
 // weight bytes per token.
 bool decode_regime(const moe_cfg_t &c, int T) { return static_cast<double>(c.topk) * T / c.E <= 12.0; }
 
-int expert_bn(const moe_cfg_t &c, int T) { return decode_regime(c, T) ? 32 : 128; }
+// Beyond 128 expected rows per expert (skewed routing, large batches) the tiles
+// widen to 192 tokens: 1.5x the MACs per TMA request.
+int wide_bn(const moe_cfg_t &c, int T) {
+    if (decode_regime(c, T)) return 32;
+    return static_cast<double>(c.topk) * T / c.E > 128.0 ? 192 : 128;
+}
 
-int down_bn(const moe_cfg_t &c, int T) { return decode_regime(c, T) ? 32 : 128; }
+int expert_bn(const moe_cfg_t &c, int T) { return wide_bn(c, T); }
+
+int down_bn(const moe_cfg_t &c, int T) { return wide_bn(c, T); }
 
 int router_bn(int T) { return T <= 512 ? 32 : 128; }
 
@@ -232,9 +239,10 @@ int make_map_gateup(CUtensorMap *m, const void *ptr, uint64_t G, uint64_t H, uin
     return MOE_OK;
 }
 
-// Activation maps with box heights 16, 32, 64 and 128 rows.
+// Activation maps with box heights 16, 32, 64, 128 and 192 rows.
 int make_act_maps(ActMaps *m, const void *ptr, int elem_bytes, uint64_t rows, uint64_t cols) {
-    for (int i = 0; i < 4; ++i) MOE_CHECK(make_map(&m->box[i], ptr, elem_bytes, rows, cols, kActBoxRows << i));
+    const uint32_t heights[5] = {16, 32, 64, 128, 192};
+    for (int i = 0; i < 5; ++i) MOE_CHECK(make_map(&m->box[i], ptr, elem_bytes, rows, cols, heights[i]));
     return MOE_OK;
 }
 
@@ -616,7 +624,7 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     gu.a_second_offset = H;
     gu.n_proj = 2;
     gu.out_f32 = gu_f32;
-    MOE_CUDA(launch_grouped_gemm(Kind::Proj, 128, m13, mx, gu, num_sms(), st), "gate/up projection launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::Proj, 192, m13, mx, gu, num_sms(), st), "gate/up projection launch");
     MOE_CUDA(launch_swiglu_quant(gu_f32, T, H, hq, hs_t, num_sms(), st), "SwiGLU quantise launch");
     GemmArgs dn{};
     dn.G = 1;
@@ -628,7 +636,7 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     dn.w_scale = w2_s;
     dn.a_rows_per_group = d;
     dn.out = static_cast<__nv_bfloat16 *>(y);
-    MOE_CUDA(launch_grouped_gemm(Kind::Down, 128, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::Down, 192, m2, mh, dn, num_sms(), st), "down GEMM launch");
     t_launches = 4;
     return MOE_OK;
 }

@@ -39,6 +39,10 @@ static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const ActMaps &ma
             if constexpr (KIND != Kind::GateUp && KIND != Kind::DownPair)
                 return launch_kind<KIND, 128>(map_a, map_b, args, grid, stream);
             break;
+        case 192:
+            if constexpr (KIND == Kind::Proj || KIND == Kind::Down)
+                return launch_kind<KIND, 192>(map_a, map_b, args, grid, stream);
+            break;
         default: break;
     }
     return cudaErrorInvalidValue;

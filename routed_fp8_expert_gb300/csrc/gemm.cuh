@@ -11,8 +11,9 @@
 //               TMA tile loads (weight tile(s) + activation rows per 128-byte K
 //               block) and copies the scales of each stage
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..9  epilogue: 2 column groups of four warps; each warp reads its
-//               32-lane quarter of TMEM for its group's token columns
+//   warps 2..   epilogue: 2 column groups of four warps (3 groups for 192-token
+//               tiles); each warp reads its 32-lane quarter of TMEM for its
+//               group's token columns
 //   last warp   (FP8 kinds) copies each K block's activation and weight scales
 //
 // Tile scheduler: for expert groups the producer takes the next item from a
@@ -53,6 +54,7 @@ constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
 constexpr int kATileBytes = kBM * kKBytes;  // 16 KB
 constexpr int kActBoxRows = 16;             // smallest activation TMA box height
+__device__ constexpr int kActBoxHeights[5] = {16, 32, 64, 128, 192};
 constexpr int kMaxGroups = 1032;            // routed + shared experts, padded
 constexpr int kItemQ = 4;                   // depth of the producer -> consumers item queue
 
@@ -68,7 +70,9 @@ template <Kind K, int BN> struct KindCfg {
     static constexpr bool kBf16 = (K == Kind::Router);
     static constexpr int kBTileBytes = BN * kKBytes;
     static constexpr int kStageBytes = kATiles * kATileBytes + kBTileBytes;
-    static constexpr int kStages = (kStageBudget / kStageBytes) > 12 ? 12 : (kStageBudget / kStageBytes);
+    // wide tiles leave room for their larger epilogue slots
+    static constexpr int kBudget = BN >= 192 ? 184 * 1024 : kStageBudget;
+    static constexpr int kStages = (kBudget / kStageBytes) > 12 ? 12 : (kBudget / kStageBytes);
     static constexpr int kPartCols = kATiles * BN;                // one TMEM partial buffer
     // partial buffers in flight between the MMA issuer and the epilogue: as
     // many as TMEM holds, up to 4, so the MMAs run ahead of the promotion
@@ -77,13 +81,15 @@ template <Kind K, int BN> struct KindCfg {
     // scale slots: their own ring, released by the epilogue, so operand stages
     // are released by the MMA alone and the producer keeps kStages ahead of it
     static constexpr int kScaleSlots = kPromote ? (kStages + kNumPart + 2) : 1;
-    static constexpr int kGroups = 2;                              // epilogue column groups
+    // epilogue column groups: three (12 warps) for the single-accumulator kinds at
+    // 192-token tiles, so 64 accumulator columns per thread; two otherwise
+    static constexpr int kGroups = (kATiles == 1 && kPromote && BN == 192) ? 3 : 2;
     static constexpr int kHalfCols = BN / kGroups;                // token columns per column group
     static constexpr int kChunks = kHalfCols / 16;
     static constexpr int kEpiWarps = 4 * kGroups;                 // one warp per TMEM lane quarter and group
     static constexpr int kScaleWarp = 2 + kEpiWarps;               // copies the K blocks' scales
     static constexpr int kThreads = 64 + 32 * kEpiWarps + (kPromote ? 32 : 0);
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 192, "tile width");
     static_assert(kStages >= 3, "pipeline depth");
 };
 
@@ -264,7 +270,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&map_a);
-        for (int i = 0; i < 4; ++i) tma_prefetch_desc(&map_b.box[i]);
+        for (int i = 0; i < 5; ++i) tma_prefetch_desc(&map_b.box[i]);
     }
     if (warp == 1) tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
     tc_fence_before();
@@ -321,9 +327,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             }
             int kb0, kb1;
             kb_range(args, I, kb0, kb1);
-            // one activation box: the smallest of 16/32/64/128 rows that covers the tile
-            const int box_i = (I.n <= 16) ? 0 : (I.n <= 32) ? 1 : (I.n <= 64) ? 2 : 3;
-            const uint32_t bytes = C::kATiles * kATileBytes + (kActBoxRows << box_i) * kKBytes;
+            // one activation box: the smallest of 16/32/64/128/192 rows that covers the tile
+            const int box_i = (I.n <= 16) ? 0 : (I.n <= 32) ? 1 : (I.n <= 64) ? 2 : (I.n <= 128) ? 3 : 4;
+            const uint32_t bytes = C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes;
             const uint64_t pol_w = (I.ntiles > 1) ? pol_shared : pol_stream;
             int arow0;
             if constexpr (KIND == Kind::Router) {
@@ -489,21 +495,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             const int n_my = max(0, min(HC, I.n - col_base));
             if constexpr (C::kPromote) {
                 constexpr bool kTwo = (C::kATiles == 2);
-                float acc0[HC], acc1[HC];
+                float acc0[HC], acc1[kTwo ? HC : 1];
 #pragma unroll
-                for (int j = 0; j < HC; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
+                for (int j = 0; j < HC; ++j) acc0[j] = 0.f;
+                if constexpr (kTwo) {
+#pragma unroll
+                    for (int j = 0; j < HC; ++j) acc1[j] = 0.f;
+                }
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     // 1. wait for this K block's partial products, start loading them
                     if (!mbar_wait(smem_u32(&pfull[pbuf]), pphase, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t tcol = t_lane + pbuf * C::kPartCols + col_base;
-                    float p[C::kATiles][C::kChunks][16];
-                    if (n_my > 0) {
+                    // the partial's 16-column chunks (gate first, then up for the
+                    // two-tile kinds) are loaded kLd at a time: all of them when the
+                    // registers allow, one at a time in the wide (16-warp) epilogue
+                    constexpr int kTot = C::kATiles * C::kChunks;
+                    constexpr int kLd = (C::kThreads > 384) ? 1 : kTot;
+                    float p[kLd][16];
+                    auto load_batch = [&](int t0) {
 #pragma unroll
-                        for (int pass = 0; pass < C::kATiles; ++pass)
-#pragma unroll
-                            for (int c = 0; c < C::kChunks; ++c) tmem_ld16(tcol + pass * BN + c * 16, p[pass][c]);
-                    }
+                        for (int b = 0; b < kLd; ++b) {
+                            const int t = t0 + b;
+                            tmem_ld16(tcol + (t / C::kChunks) * BN + (t % C::kChunks) * 16, p[b]);
+                        }
+                    };
+                    if (n_my > 0) load_batch(0);
                     // 2. while they are in flight: the combined scales
                     //    s_w[mb, kb] * s_x[row_j, kb] of this warp's columns, once per
                     //    K block, into a warp-private slot
@@ -527,22 +544,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     __syncwarp();
                     // 3. fold the partials into the fp32 accumulators
                     if (n_my > 0) {
-                        tmem_wait_ld();
 #pragma unroll
-                        for (int pass = 0; pass < C::kATiles; ++pass) {
-                            float *acc = (pass == 0) ? acc0 : acc1;
-                            const float *cp = cs + pass * HC;
+                        for (int t0 = 0; t0 < kTot; t0 += kLd) {
+                            if (t0 > 0) load_batch(t0);
+                            tmem_wait_ld();
 #pragma unroll
-                            for (int c = 0; c < C::kChunks; ++c) {
-                                const float4 *s4 = reinterpret_cast<const float4 *>(cp + c * 16);
+                            for (int b = 0; b < kLd; ++b) {
+                                const int t = t0 + b;
+                                const int pass = t / C::kChunks, c = t % C::kChunks;
+                                float *acc = (pass == 0) ? acc0 : acc1;
+                                const float4 *s4 = reinterpret_cast<const float4 *>(cs + pass * HC + c * 16);
 #pragma unroll
                                 for (int v = 0; v < 4; ++v) {
                                     const float4 a4 = s4[v];
                                     const int j = c * 16 + v * 4;
-                                    acc[j + 0] = fmaf(a4.x, p[pass][c][v * 4 + 0], acc[j + 0]);
-                                    acc[j + 1] = fmaf(a4.y, p[pass][c][v * 4 + 1], acc[j + 1]);
-                                    acc[j + 2] = fmaf(a4.z, p[pass][c][v * 4 + 2], acc[j + 2]);
-                                    acc[j + 3] = fmaf(a4.w, p[pass][c][v * 4 + 3], acc[j + 3]);
+                                    acc[j + 0] = fmaf(a4.x, p[b][v * 4 + 0], acc[j + 0]);
+                                    acc[j + 1] = fmaf(a4.y, p[b][v * 4 + 1], acc[j + 1]);
+                                    acc[j + 2] = fmaf(a4.z, p[b][v * 4 + 2], acc[j + 2]);
+                                    acc[j + 3] = fmaf(a4.w, p[b][v * 4 + 3], acc[j + 3]);
                                 }
                             }
                         }

@@ -9,11 +9,11 @@ namespace moe {
 struct GemmArgs;
 enum class Kind;
 
-// Tensor maps of one activation matrix with box heights 16, 32, 64 and 128 rows
-// (128 bytes wide, 128-byte swizzle): a token tile is loaded with the smallest
-// single box that covers its rows.
+// Tensor maps of one activation matrix with box heights 16, 32, 64, 128 and 192
+// rows (128 bytes wide, 128-byte swizzle): a token tile is loaded with the
+// smallest single box that covers its rows.
 struct ActMaps {
-    CUtensorMap box[4];
+    CUtensorMap box[5];
 };
 
 // Grouped tcgen05 GEMM launch (gemm.cu). Returns a cudaError_t.

@@ -56,6 +56,18 @@ def test_experts_with_several_token_tiles():
     assert _run(shape, seed=1) == 9 * 400
 
 
+def test_experts_beyond_128_rows_use_192_token_tiles():
+    # 150 rows per routed expert and 600 shared rows: 192-token tiles, several per expert
+    shape = S.MoEShape("wide_tiles", T=600, d=512, E=32, topk=8, H=256)
+    assert _run(shape, seed=3, n_check=40) > 0
+
+
+def test_decode_down_with_odd_block_count():
+    # d = 384: three 128-row output blocks, so the decode down GEMM cannot pair them
+    shape = S.MoEShape("odd_d", T=8, d=384, E=16, topk=4, H=256)
+    assert _run(shape, seed=4) == 5 * 8
+
+
 def test_wide_k_and_many_blocks():
     shape = S.MoEShape("wide", T=48, d=2048, E=16, topk=4, H=640, n_shared=1)
     _run(shape, seed=2)
