@@ -87,24 +87,20 @@ int num_sms() {
 // decides. Narrow tiles leave more shared memory to the weight pipeline; the
 // 64-token tile keeps every TMEM chunk of a K block in registers at once.
 //
-// Decode regime (<= 12 expected rows per expert): 32-token tiles and the fused
-// gate/up kernel, which streams the weights at the HBM rate. Beyond it:
-// 128-token tiles, with gate and up as separate items of the single-projection
-// kernel (one accumulator per column fits 128 columns in registers), followed
-// by the SwiGLU + quantise kernel. Wide tiles halve the MMA issues and the
-// weight bytes per token.
+// Decode regime (<= 12 expected rows per expert): 32-token tiles in the swap-AB
+// kernels (weight rows on the MMA M dimension) and the fused gate/up kernel,
+// which streams the weights at the HBM rate. Beyond it: 128-token tiles in the
+// token-major kernels (tokens on M), with gate and up as separate items of the
+// single-projection kernel, followed by the SwiGLU + quantise kernel.
 bool decode_regime(const moe_cfg_t &c, int T) { return static_cast<double>(c.topk) * T / c.E <= 12.0; }
 
-// Beyond 128 expected rows per expert (skewed routing, large batches) the tiles
-// widen to 192 tokens: 1.5x the MACs per TMA request.
-int wide_bn(const moe_cfg_t &c, int T) {
-    if (decode_regime(c, T)) return 32;
-    return static_cast<double>(c.topk) * T / c.E > 128.0 ? 192 : 128;
-}
+int expert_bn(const moe_cfg_t &c, int T) { return decode_regime(c, T) ? 32 : 128; }
 
-int expert_bn(const moe_cfg_t &c, int T) { return wide_bn(c, T); }
+// The decode down projection pairs two 128-row weight blocks per item, which
+// needs an even number of them; otherwise the token-major kernel runs.
+bool down_pair(const moe_cfg_t &c, int T) { return decode_regime(c, T) && (c.d / 128) % 2 == 0; }
 
-int down_bn(const moe_cfg_t &c, int T) { return wide_bn(c, T); }
+int down_bn(const moe_cfg_t &c, int T) { return down_pair(c, T) ? 32 : 128; }
 
 int router_bn(int T) { return T <= 512 ? 32 : 128; }
 
@@ -239,10 +235,35 @@ int make_map_gateup(CUtensorMap *m, const void *ptr, uint64_t G, uint64_t H, uin
     return MOE_OK;
 }
 
-// Activation maps with box heights 16, 32, 64, 128 and 192 rows.
+// Activation maps with box heights 16, 32, 64 and 128 rows.
 int make_act_maps(ActMaps *m, const void *ptr, int elem_bytes, uint64_t rows, uint64_t cols) {
-    const uint32_t heights[5] = {16, 32, 64, 128, 192};
-    for (int i = 0; i < 5; ++i) MOE_CHECK(make_map(&m->box[i], ptr, elem_bytes, rows, cols, heights[i]));
+    const uint32_t heights[kActBoxes] = {16, 32, 64, 128};
+    for (int i = 0; i < kActBoxes; ++i) MOE_CHECK(make_map(&m->box[i], ptr, elem_bytes, rows, cols, heights[i]));
+    return MOE_OK;
+}
+
+// An FP8 matrix [rows][cols] viewed as 3D (x = byte inside a 128-byte K block,
+// y = row, z = K block) so that one box {128, box_rows, 2} holds two consecutive
+// K blocks of box_rows rows: in shared memory, two 128-byte-swizzled K-major
+// tiles one after the other. A box that starts at the last K block of an odd
+// count reads zeros for the second.
+int make_map_kpair(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[3] = {128, rows, cols / 128};
+    cuuint64_t strides[2] = {cols, 128};
+    cuuint32_t box[3] = {128, box_rows, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (K pairs) failed (%d)", static_cast<int>(r));
+    return MOE_OK;
+}
+
+int make_act_maps_kpair(ActMaps *m, const void *ptr, uint64_t rows, uint64_t cols) {
+    const uint32_t heights[kActBoxes] = {16, 32, 64, 128};
+    for (int i = 0; i < kActBoxes; ++i) MOE_CHECK(make_map_kpair(&m->box[i], ptr, rows, cols, heights[i]));
     return MOE_OK;
 }
 
@@ -312,6 +333,8 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     gu.n_proj = 2;
     gu.out_f32 = ws.gu;
     gu.item_counter = ws.counters;
+    MOE_CHECK(make_map_kpair(&m13, w13, static_cast<uint64_t>(G) * 2 * c.H, c.d, kBM));
+    MOE_CHECK(make_act_maps_kpair(&mx, xq_perm, R, c.d));
     MOE_CUDA(launch_grouped_gemm(Kind::Proj, bn, m13, mx, gu, num_sms(), st), "gate/up projection launch");
     MOE_CUDA(launch_swiglu_quant(ws.gu, R, c.H, hq, hs, num_sms(), st), "SwiGLU quantise launch");
     t_launches += 2;
@@ -346,7 +369,7 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
     dn.w_scale = w2_s;
     dn.a_rows_per_group = c.d;
     dn.out = static_cast<__nv_bfloat16 *>(o);
-    if (decode_regime(c, T) && (c.d / 128) % 2 == 0) {
+    if (down_pair(c, T)) {
         // decode: two adjacent 128-row blocks per item, one 256-row box (32 KB of
         // weights per K block and request)
         MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
@@ -354,6 +377,8 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
         dn.a_second_offset = kBM;
         MOE_CUDA(launch_grouped_gemm(Kind::DownPair, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     } else {
+        MOE_CHECK(make_map_kpair(&m2, w2, static_cast<uint64_t>(G) * c.d, c.H, kBM));
+        MOE_CHECK(make_act_maps_kpair(&mh, hq, R, c.H));
         MOE_CUDA(launch_grouped_gemm(Kind::Down, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     }
     t_launches += 1;
@@ -608,10 +633,10 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     MOE_CUDA(launch_quant(x, true, T, d, xq, sx_t, true, num_sms(), st), "quantise launch");
     CUtensorMap m13, m2;
     ActMaps mx, mh;
-    MOE_CHECK(make_map(&m13, w13, 1, static_cast<uint64_t>(2) * H, d, kBM));
-    MOE_CHECK(make_act_maps(&mx, xq, 1, T, d));
-    MOE_CHECK(make_map(&m2, w2, 1, d, H, kBM));
-    MOE_CHECK(make_act_maps(&mh, hq, 1, T, H));
+    MOE_CHECK(make_map_kpair(&m13, w13, static_cast<uint64_t>(2) * H, d, kBM));
+    MOE_CHECK(make_act_maps_kpair(&mx, xq, T, d));
+    MOE_CHECK(make_map_kpair(&m2, w2, d, H, kBM));
+    MOE_CHECK(make_act_maps_kpair(&mh, hq, T, H));
     GemmArgs gu{};
     gu.G = 1;
     gu.num_kb = d / 128;
@@ -624,7 +649,7 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     gu.a_second_offset = H;
     gu.n_proj = 2;
     gu.out_f32 = gu_f32;
-    MOE_CUDA(launch_grouped_gemm(Kind::Proj, 192, m13, mx, gu, num_sms(), st), "gate/up projection launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::Proj, 128, m13, mx, gu, num_sms(), st), "gate/up projection launch");
     MOE_CUDA(launch_swiglu_quant(gu_f32, T, H, hq, hs_t, num_sms(), st), "SwiGLU quantise launch");
     GemmArgs dn{};
     dn.G = 1;
@@ -636,7 +661,7 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     dn.w_scale = w2_s;
     dn.a_rows_per_group = d;
     dn.out = static_cast<__nv_bfloat16 *>(y);
-    MOE_CUDA(launch_grouped_gemm(Kind::Down, 192, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    MOE_CUDA(launch_grouped_gemm(Kind::Down, 128, m2, mh, dn, num_sms(), st), "down GEMM launch");
     t_launches = 4;
     return MOE_OK;
 }

@@ -21,27 +21,19 @@ static cudaError_t launch_kind(const CUtensorMap &map_a, const ActMaps &map_b, c
     return cudaGetLastError();
 }
 
-// Token-tile widths compiled per kind: the fused gate/up epilogue holds two
-// accumulators per column and serves the decode-sized tiles; the
-// single-projection kind serves the 128-token tiles.
+// Token-tile widths compiled per kind: the swap-AB kinds serve decode-sized
+// tiles (32 tokens; the router also 128), the token-major kinds 128-token tiles.
 template <Kind KIND>
 static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const ActMaps &map_b, const GemmArgs &args,
                              int grid, cudaStream_t stream) {
+    constexpr bool kTokenMajor = (KIND == Kind::Proj || KIND == Kind::Down);
     switch (bn) {
         case 32:
-            if constexpr (KIND != Kind::Proj) return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
-            break;
-        case 64:
-            if constexpr (KIND != Kind::Proj && KIND != Kind::DownPair)
-                return launch_kind<KIND, 64>(map_a, map_b, args, grid, stream);
+            if constexpr (!kTokenMajor) return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
             break;
         case 128:
-            if constexpr (KIND != Kind::GateUp && KIND != Kind::DownPair)
+            if constexpr (kTokenMajor || KIND == Kind::Router)
                 return launch_kind<KIND, 128>(map_a, map_b, args, grid, stream);
-            break;
-        case 192:
-            if constexpr (KIND == Kind::Proj || KIND == Kind::Down)
-                return launch_kind<KIND, 192>(map_a, map_b, args, grid, stream);
             break;
         default: break;
     }

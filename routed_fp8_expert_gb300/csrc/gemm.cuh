@@ -1,19 +1,23 @@
 // Persistent grouped GEMM on the tcgen05 tensor cores (sm_103a).
 //
-// Swap-AB formulation: the weight rows of one 128-row block are the MMA M
-// dimension (TMEM lanes) and the tokens of one segment tile are the MMA N
-// dimension (TMEM columns). A "work item" is (group g, 128-row weight block mb,
-// token tile nt); items of one group are ordered mb-major so that the token
-// tiles sharing a weight block run at the same time on neighbouring CTAs.
+// A "work item" is (group g, 128-row weight block mb, token tile nt); items of
+// one group are ordered mb-major so that the token tiles sharing a weight block
+// run at the same time on neighbouring CTAs. Two orientations:
+//   swap-AB (decode-sized tiles: GateUp, DownPair, Router): the block's weight
+//     rows are the MMA M dimension (TMEM lanes) and the tile's tokens the N
+//     dimension (TMEM columns), so a handful of tokens costs an N=16 MMA;
+//   token-major (128-token tiles: Proj, Down): the tile's 128 tokens are M and
+//     the block's 128 weight rows N. Each epilogue thread then owns one token,
+//     and the per-K-block scale s_w[mb,kb] * s_x[token,kb] is one scalar per
+//     thread instead of one value per column.
 //
 // Roles (one CTA per SM):
 //   warp 0      producer: takes work items from the tile scheduler, issues the
 //               TMA tile loads (weight tile(s) + activation rows per 128-byte K
-//               block) and copies the scales of each stage
+//               block, or per pair of K blocks for the token-major kinds)
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..   epilogue: 2 column groups of four warps (3 groups for 192-token
-//               tiles); each warp reads its 32-lane quarter of TMEM for its
-//               group's token columns
+//   warps 2..9  epilogue: 2 column groups of four warps; each warp reads its
+//               32-lane quarter of TMEM for its group's columns
 //   last warp   (FP8 kinds) copies each K block's activation and weight scales
 //
 // Tile scheduler: for expert groups the producer takes the next item from a
@@ -40,10 +44,10 @@
 namespace moe {
 
 // GateUp: gate and up projections of one weight block, fused SiLU*mul and h quantisation.
-// Proj:   one projection (gate or up) per item, fp32 output; SiLU*mul and h
-//         quantisation follow in a separate kernel. Items carry half the weight
-//         tiles of GateUp, so 128-token tiles fit the epilogue's registers.
-// Down:   down projection, bf16 output.
+// Proj:   one projection (gate or up) per item, token-major, fp32 output; SiLU*mul
+//         and h quantisation follow in a separate kernel. Items carry half the
+//         weight tiles of GateUp, so 128-token tiles fit the epilogue's registers.
+// Down:   down projection, token-major, bf16 output.
 // DownPair: down projection with two adjacent 128-row weight blocks per item
 //         (like GateUp's two tiles): twice the weight bytes per K block for the
 //         same per-K-block fixed costs; used for decode-sized tiles.
@@ -54,7 +58,7 @@ constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
 constexpr int kATileBytes = kBM * kKBytes;  // 16 KB
 constexpr int kActBoxRows = 16;             // smallest activation TMA box height
-__device__ constexpr int kActBoxHeights[5] = {16, 32, 64, 128, 192};
+__device__ constexpr int kActBoxHeights[kActBoxes] = {16, 32, 64, 128};
 constexpr int kMaxGroups = 1032;            // routed + shared experts, padded
 constexpr int kItemQ = 4;                   // depth of the producer -> consumers item queue
 
@@ -68,12 +72,16 @@ template <Kind K, int BN> struct KindCfg {
     static constexpr int kATiles = (K == Kind::GateUp || K == Kind::DownPair) ? 2 : 1;
     static constexpr bool kPromote = (K != Kind::Router);         // per-128-K fp32 promotion
     static constexpr bool kBf16 = (K == Kind::Router);
+    // token-major: tokens on the TMEM lanes (M = 128), weight rows on the columns
+    static constexpr bool kTM = (K == Kind::Proj || K == Kind::Down);
+    // K blocks per stage: the single-tile FP8 kinds load two consecutive K blocks
+    // per TMA request (3D maps with a K-block dimension), halving the requests
+    static constexpr int kKPS = (K == Kind::Proj || K == Kind::Down) ? 2 : 1;
     static constexpr int kBTileBytes = BN * kKBytes;
-    static constexpr int kStageBytes = kATiles * kATileBytes + kBTileBytes;
-    // wide tiles leave room for their larger epilogue slots
-    static constexpr int kBudget = BN >= 192 ? 184 * 1024 : kStageBudget;
-    static constexpr int kStages = (kBudget / kStageBytes) > 12 ? 12 : (kBudget / kStageBytes);
-    static constexpr int kPartCols = kATiles * BN;                // one TMEM partial buffer
+    static constexpr int kAStageBytes = kKPS * kATiles * kATileBytes;   // weight part of a stage
+    static constexpr int kStageBytes = kAStageBytes + kKPS * kBTileBytes;
+    static constexpr int kStages = (kStageBudget / kStageBytes) > 12 ? 12 : (kStageBudget / kStageBytes);
+    static constexpr int kPartCols = kTM ? kBM : kATiles * BN;    // one TMEM partial buffer
     // partial buffers in flight between the MMA issuer and the epilogue: as
     // many as TMEM holds, up to 4, so the MMAs run ahead of the promotion
     static constexpr int kNumPart = (512 / kPartCols) >= 4 ? 4 : (512 / kPartCols);
@@ -81,16 +89,17 @@ template <Kind K, int BN> struct KindCfg {
     // scale slots: their own ring, released by the epilogue, so operand stages
     // are released by the MMA alone and the producer keeps kStages ahead of it
     static constexpr int kScaleSlots = kPromote ? (kStages + kNumPart + 2) : 1;
-    // epilogue column groups: three (12 warps) for the single-accumulator kinds at
-    // 192-token tiles, so 64 accumulator columns per thread; two otherwise
-    static constexpr int kGroups = (kATiles == 1 && kPromote && BN == 192) ? 3 : 2;
-    static constexpr int kHalfCols = BN / kGroups;                // token columns per column group
+    // epilogue column groups: token columns (swap-AB) or weight rows (token-major)
+    static constexpr int kGroups = 2;
+    static constexpr int kHalfCols = (kTM ? kBM : BN) / kGroups;  // columns per column group
     static constexpr int kChunks = kHalfCols / 16;
     static constexpr int kEpiWarps = 4 * kGroups;                 // one warp per TMEM lane quarter and group
     static constexpr int kScaleWarp = 2 + kEpiWarps;               // copies the K blocks' scales
     static constexpr int kThreads = 64 + 32 * kEpiWarps + (kPromote ? 32 : 0);
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 192, "tile width");
-    static_assert(kStages >= 3, "pipeline depth");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
+    static_assert(!kTM || BN == 128, "token-major tiles hold 128 tokens (the MMA M dimension)");
+    static_assert(kStages * kKPS >= 4 && kStages >= 2, "pipeline depth");
+    static_assert(kKPS == 1 || kATiles == 1, "K-pair stages hold one weight tile per K block");
 };
 
 struct GemmArgs {
@@ -182,6 +191,21 @@ __device__ __forceinline__ void kb_range(const GemmArgs &a, const Item &I, int &
     kb1 = (a.num_kb * (I.ks + 1)) / splits;
 }
 
+// Index into kActBoxHeights of the activation box of a tile of n rows: the
+// smallest that covers them, or the 128-row box (the MMA M dimension) for the
+// token-major kinds.
+template <bool kTokenMajor>
+__device__ __forceinline__ int act_box_index(int n) {
+    if (kTokenMajor) return 3;
+    return (n <= 16) ? 0 : (n <= 32) ? 1 : (n <= 64) ? 2 : 3;
+}
+
+// Two floats as round-to-nearest bf16, the first in the low half (lower address).
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // Shared-memory carve-up of one CTA (offsets from a 1024-byte aligned base).
@@ -270,7 +294,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&map_a);
-        for (int i = 0; i < 5; ++i) tma_prefetch_desc(&map_b.box[i]);
+        for (int i = 0; i < kActBoxes; ++i) tma_prefetch_desc(&map_b.box[i]);
     }
     if (warp == 1) tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
     tc_fence_before();
@@ -327,9 +351,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             }
             int kb0, kb1;
             kb_range(args, I, kb0, kb1);
-            // one activation box: the smallest of 16/32/64/128/192 rows that covers the tile
-            const int box_i = (I.n <= 16) ? 0 : (I.n <= 32) ? 1 : (I.n <= 64) ? 2 : (I.n <= 128) ? 3 : 4;
-            const uint32_t bytes = C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes;
+            // one activation box per stage
+            const int box_i = act_box_index<C::kTM>(I.n);
+            // full boxes count toward the transaction bytes, including rows and a
+            // K block beyond the tensor, which the TMA unit fills with zeros
+            const uint32_t bytes = C::kKPS * (C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes);
             const uint64_t pol_w = (I.ntiles > 1) ? pol_shared : pol_stream;
             int arow0;
             if constexpr (KIND == Kind::Router) {
@@ -340,7 +366,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 if constexpr (KIND == Kind::Proj) arow0 += I.proj * args.a_second_offset;
             }
             bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            for (int kb = kb0; kb < kb1; kb += C::kKPS) {
                 int w = 1;
                 if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
                 w = __shfl_sync(0xffffffffu, w, 0);
@@ -349,15 +375,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, bytes);
-                    const int kx = kb * kKbElems;
                     // weight tiles in one request (the TMA unit's request rate, not its
                     // bytes, bounds an SM's loads): GateUp's gate and up tiles as one
                     // 3D box, DownPair's two row blocks as one 256-row box
-                    if constexpr (KIND == Kind::GateUp)
-                        tma_load_3d(sbase, &map_a, fb, kx, I.mb * kBM, 2 * I.g, pol_w);
-                    else
-                        tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
-                    tma_load_2d(sbase + C::kATiles * kATileBytes, &map_b.box[box_i], fb, kx, I.row0, pol_x);
+                    // K-pair kinds: K blocks kb and kb+1 of the weight rows and of the
+                    // activation rows, one request each (x = 0, y = row, z = K block)
+                    if constexpr (C::kKPS == 2) {
+                        tma_load_3d(sbase, &map_a, fb, 0, arow0, kb, pol_w);
+                        tma_load_3d(sbase + C::kAStageBytes, &map_b.box[box_i], fb, 0, I.row0, kb, pol_x);
+                    } else {
+                        const int kx = kb * kKbElems;
+                        if constexpr (KIND == Kind::GateUp)
+                            tma_load_3d(sbase, &map_a, fb, kx, I.mb * kBM, 2 * I.g, pol_w);
+                        else
+                            tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
+                        tma_load_2d(sbase + C::kAStageBytes, &map_b.box[box_i], fb, kx, I.row0, pol_x);
+                    }
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -386,35 +419,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
                 int kb0, kb1;
                 kb_range(args, I, kb0, kb1);
-                const int n_mma = (I.n + 15) & ~15;
+                // swap-AB: M = 128 weight rows, N = the tile's tokens rounded up to 16;
+                // token-major: M = 128 tokens, N = 128 weight rows
+                const int n_mma = C::kTM ? kBM : ((I.n + 15) & ~15);
                 const uint32_t idesc = idesc_make(kFmt, kFmt, kBM, n_mma);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                // bytes of one K block's activation sub-tile inside a K-pair box
+                const uint32_t b_kb_bytes = kActBoxHeights[act_box_index<C::kTM>(I.n)] * kKBytes;
+                for (int kb = kb0; kb < kb1; kb += C::kKPS) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) { ok = false; break; }
-                    if (C::kPromote || kb == kb0) {
-                        if (!mbar_wait(smem_u32(&pempty[pbuf]), pphase ^ 1, abort_flag, args.err, ERR_WAIT_PART_EMPTY)) {
-                            ok = false;
-                            break;
+                    const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
+#pragma unroll
+                    for (int h = 0; h < C::kKPS; ++h) {
+                        const int kbh = kb + h;
+                        if (kbh >= kb1) break;   // odd K-block count: the pair's second half is padding
+                        if (C::kPromote || kbh == kb0) {
+                            if (!mbar_wait(smem_u32(&pempty[pbuf]), pphase ^ 1, abort_flag, args.err, ERR_WAIT_PART_EMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        tc_fence_after();
+                        const uint32_t abase = sbase + h * C::kATiles * kATileBytes;
+                        const uint32_t bbase = sbase + C::kAStageBytes + h * b_kb_bytes;
+                        const uint32_t dcol = tmem_base + pbuf * C::kPartCols;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t acc = C::kPromote ? (k > 0) : (kbh > kb0 || k > 0);
+                            const uint64_t bdesc = sdesc_sw128(bbase + k * 32);   // activations
+                            const uint64_t adesc = sdesc_sw128(abase + k * 32);   // weights
+                            if constexpr (C::kBf16) mma_bf16(dcol, adesc, bdesc, idesc, acc);
+                            else if constexpr (C::kTM) mma_f8(dcol, bdesc, adesc, idesc, acc);
+                            else mma_f8(dcol, adesc, bdesc, idesc, acc);
+                            if constexpr (C::kATiles == 2)
+                                mma_f8(dcol + BN, sdesc_sw128(abase + kATileBytes + k * 32), bdesc, idesc, acc);
+                        }
+                        if (C::kPromote || kbh == kb1 - 1) {
+                            mma_commit(smem_u32(&pfull[pbuf]));
+                            if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
                         }
                     }
-                    tc_fence_after();
-                    const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
-                    const uint32_t bbase = sbase + C::kATiles * kATileBytes;
-                    const uint32_t dcol = tmem_base + pbuf * C::kPartCols;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t acc = C::kPromote ? (k > 0) : (kb > kb0 || k > 0);
-                        const uint64_t bdesc = sdesc_sw128(bbase + k * 32);
-                        const uint64_t adesc = sdesc_sw128(sbase + k * 32);
-                        if constexpr (C::kBf16) mma_bf16(dcol, adesc, bdesc, idesc, acc);
-                        else mma_f8(dcol, adesc, bdesc, idesc, acc);
-                        if constexpr (C::kATiles == 2)
-                            mma_f8(dcol + BN, sdesc_sw128(sbase + kATileBytes + k * 32), bdesc, idesc, acc);
-                    }
+                    if (!ok) break;
                     mma_commit(smem_u32(&empty[stage]));
-                    if (C::kPromote || kb == kb1 - 1) {
-                        mma_commit(smem_u32(&pfull[pbuf]));
-                        if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
-                    }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
             }
@@ -493,7 +538,70 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             Item I;
             if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
             const int n_my = max(0, min(HC, I.n - col_base));
-            if constexpr (C::kPromote) {
+            if constexpr (C::kTM) {
+                // token-major: this thread's TMEM lane is token row r of the tile, its
+                // columns the weight rows [col_base, col_base + 64) of block mb
+                const int r = quad * 32 + lane;
+                float acc[HC];
+#pragma unroll
+                for (int j = 0; j < HC; ++j) acc[j] = 0.f;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&pfull[pbuf]), pphase, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t tcol = t_lane + pbuf * C::kPartCols + col_base;
+                    float p[C::kChunks][16];
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c) tmem_ld16(tcol + c * 16, p[c]);
+                    // while the loads are in flight: this token's scale for the K block,
+                    // s_w[mb, kb] * s_x[row r, kb] (rows beyond the tile's end compute on
+                    // stale slot entries and are never stored)
+                    if (!mbar_wait(smem_u32(&sfull[sslot]), sphase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) {
+                        tmem_wait_ld();
+                        ok = false;
+                        break;
+                    }
+                    const float *sc = s_scale + sslot * L::kScaleStride;
+                    const float s_kb = sc[BN] * sc[r];
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s_kb, p[c][i], acc[c * 16 + i]);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&pempty[pbuf]));
+                        mbar_arrive(smem_u32(&sempty[sslot]));
+                    }
+                    if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
+                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
+                }
+                if (!ok) break;
+                if (r < I.n) {
+                    // one token's 64 consecutive outputs: 16-byte stores
+                    const size_t row = static_cast<size_t>(I.row0 + r);
+                    const int nout = args.num_mb * kBM;   // output features per row
+                    const size_t col = static_cast<size_t>(I.mb) * kBM + col_base;
+                    if constexpr (KIND == Kind::Proj) {
+                        float4 *d4 = reinterpret_cast<float4 *>(
+                            args.out_f32 + (static_cast<size_t>(I.proj) * args.total_rows + row) * nout + col);
+#pragma unroll
+                        for (int v = 0; v < HC / 4; ++v)
+                            d4[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+                    } else {
+                        uint4 *o4 = reinterpret_cast<uint4 *>(args.out + row * nout + col);
+#pragma unroll
+                        for (int v = 0; v < HC / 8; ++v) {
+                            uint4 w;
+                            w.x = bf16x2_bits(acc[8 * v + 0], acc[8 * v + 1]);
+                            w.y = bf16x2_bits(acc[8 * v + 2], acc[8 * v + 3]);
+                            w.z = bf16x2_bits(acc[8 * v + 4], acc[8 * v + 5]);
+                            w.w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
+                            o4[v] = w;
+                        }
+                    }
+                }
+            } else if constexpr (C::kPromote) {
                 constexpr bool kTwo = (C::kATiles == 2);
                 float acc0[HC], acc1[kTwo ? HC : 1];
 #pragma unroll
@@ -511,7 +619,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     // two-tile kinds) are loaded kLd at a time: all of them when the
                     // registers allow, one at a time in the wide (16-warp) epilogue
                     constexpr int kTot = C::kATiles * C::kChunks;
-                    constexpr int kLd = (C::kThreads > 384) ? 1 : kTot;
+                    constexpr int kLd = (C::kThreads > 384) ? 2 : kTot;
                     float p[kLd][16];
                     auto load_batch = [&](int t0) {
 #pragma unroll
@@ -605,17 +713,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                             if (wrow == 0) args.hs_t[static_cast<size_t>(I.mb) * args.total_rows + row] = s;
                         }
                     }
-                } else if constexpr (KIND == Kind::Proj) {
-                    const int H = args.num_mb * kBM;
-                    float *dst = args.out_f32 + static_cast<size_t>(I.proj) * args.total_rows * H;
-#pragma unroll
-                    for (int j = 0; j < HC; ++j) {
-                        if (j < n_my) {
-                            const size_t row = static_cast<size_t>(I.row0 + col_base + j);
-                            dst[row * H + I.mb * kBM + wrow] = acc0[j];
-                        }
-                    }
-                } else if constexpr (KIND == Kind::DownPair) {
+                } else {
+                    static_assert(KIND == Kind::DownPair, "swap-AB promoted kinds: GateUp, DownPair");
                     const int dout = args.num_mb * 2 * kBM;
 #pragma unroll
                     for (int j = 0; j < HC; ++j) {
@@ -624,15 +723,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                             __nv_bfloat16 *o = args.out + row * dout + I.mb * 2 * kBM + wrow;
                             o[0] = __float2bfloat16_rn(acc0[j]);
                             o[kBM] = __float2bfloat16_rn(acc1[j]);
-                        }
-                    }
-                } else {
-                    const int dout = args.num_mb * kBM;
-#pragma unroll
-                    for (int j = 0; j < HC; ++j) {
-                        if (j < n_my) {
-                            const size_t row = static_cast<size_t>(I.row0 + col_base + j);
-                            args.out[row * dout + I.mb * kBM + wrow] = __float2bfloat16_rn(acc0[j]);
                         }
                     }
                 }

@@ -9,11 +9,13 @@ namespace moe {
 struct GemmArgs;
 enum class Kind;
 
-// Tensor maps of one activation matrix with box heights 16, 32, 64, 128 and 192
-// rows (128 bytes wide, 128-byte swizzle): a token tile is loaded with the
-// smallest single box that covers its rows.
+// Tensor maps of one activation matrix with box heights 16, 32, 64 and 128 rows
+// (128-byte swizzle; one K block, or a pair of K blocks for the token-major
+// kinds): a decode-sized token tile is loaded with the smallest single box that
+// covers its rows, a token-major tile with the 128-row box.
+constexpr int kActBoxes = 4;
 struct ActMaps {
-    CUtensorMap box[5];
+    CUtensorMap box[kActBoxes];
 };
 
 // Grouped tcgen05 GEMM launch (gemm.cu). Returns a cudaError_t.

@@ -65,6 +65,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is still open is suspended until
+// the phase completes or `hint_ns` nanoseconds pass, instead of returning at
+// once: a waiting warp then neither takes issue slots nor shared-memory
+// wavefronts from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest single suspension of a waiting thread; the give-up checks run between
+// suspensions.
+constexpr uint32_t kWaitSleepNs = 200000;
+
 // Wait until the phase with the given parity has completed. Gives up when
 // *abort becomes non-zero (another role gave up) or after kWaitLimitNs, in
 // which case it raises *abort and records `err_bit`. Returns false on give-up.
@@ -73,7 +93,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *abort = 1;
@@ -86,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Bounded wait that ignores the abort flag (used to drain in-flight work).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned int *err) {
     const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) {
         if (globaltimer() - t0 > kWaitLimitNs) {
             record_error(err, ERR_WAIT_DRAIN);
             return false;

@@ -56,8 +56,8 @@ def test_experts_with_several_token_tiles():
     assert _run(shape, seed=1) == 9 * 400
 
 
-def test_experts_beyond_128_rows_use_192_token_tiles():
-    # 150 rows per routed expert and 600 shared rows: 192-token tiles, several per expert
+def test_experts_beyond_128_rows_span_several_token_tiles():
+    # 150 rows per routed expert and 600 shared rows: two or more 128-token tiles per expert
     shape = S.MoEShape("wide_tiles", T=600, d=512, E=32, topk=8, H=256)
     assert _run(shape, seed=3, n_check=40) > 0
 
