@@ -330,14 +330,14 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
         t_launches += 1;
         return MOE_OK;
     }
-    gu.n_proj = 2;
-    gu.out_f32 = ws.gu;
+    // 128-token tiles, token-major: the gate and up blocks of 128 features per
+    // item (N = 256) with the fused SiLU*mul and h quantisation
+    MOE_CHECK(make_map_gateup(&m13, w13, G, c.H, c.d));
+    gu.hq = hq;
+    gu.hs_t = hs;
     gu.item_counter = ws.counters;
-    MOE_CHECK(make_map_kpair(&m13, w13, static_cast<uint64_t>(G) * 2 * c.H, c.d, kBM));
-    MOE_CHECK(make_act_maps_kpair(&mx, xq_perm, R, c.d));
-    MOE_CUDA(launch_grouped_gemm(Kind::Proj, bn, m13, mx, gu, num_sms(), st), "gate/up projection launch");
-    MOE_CUDA(launch_swiglu_quant(ws.gu, R, c.H, hq, hs, num_sms(), st), "SwiGLU quantise launch");
-    t_launches += 2;
+    MOE_CUDA(launch_grouped_gemm(Kind::GateUpWide, bn, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
+    t_launches += 1;
     return MOE_OK;
 }
 
@@ -376,6 +376,11 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
         dn.num_mb = c.d / 256;
         dn.a_second_offset = kBM;
         MOE_CUDA(launch_grouped_gemm(Kind::DownPair, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    } else if ((c.d / 128) % 2 == 0) {
+        // 128-token tiles, token-major, two 128-row blocks per item (N = 256)
+        MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
+        dn.num_mb = c.d / 256;
+        MOE_CUDA(launch_grouped_gemm(Kind::DownWide, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     } else {
         MOE_CHECK(make_map_kpair(&m2, w2, static_cast<uint64_t>(G) * c.d, c.H, kBM));
         MOE_CHECK(make_act_maps_kpair(&mh, hq, R, c.H));
@@ -633,10 +638,16 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     MOE_CUDA(launch_quant(x, true, T, d, xq, sx_t, true, num_sms(), st), "quantise launch");
     CUtensorMap m13, m2;
     ActMaps mx, mh;
-    MOE_CHECK(make_map_kpair(&m13, w13, static_cast<uint64_t>(2) * H, d, kBM));
-    MOE_CHECK(make_act_maps_kpair(&mx, xq, T, d));
-    MOE_CHECK(make_map_kpair(&m2, w2, d, H, kBM));
-    MOE_CHECK(make_act_maps_kpair(&mh, hq, T, H));
+    const bool down_wide = (d / 128) % 2 == 0;
+    MOE_CHECK(make_map_gateup(&m13, w13, 1, H, d));
+    MOE_CHECK(make_act_maps(&mx, xq, 1, T, d));
+    if (down_wide) {
+        MOE_CHECK(make_map(&m2, w2, 1, d, H, 2 * kBM));
+        MOE_CHECK(make_act_maps(&mh, hq, 1, T, H));
+    } else {
+        MOE_CHECK(make_map_kpair(&m2, w2, d, H, kBM));
+        MOE_CHECK(make_act_maps_kpair(&mh, hq, T, H));
+    }
     GemmArgs gu{};
     gu.G = 1;
     gu.num_kb = d / 128;
@@ -647,10 +658,9 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * H;
     gu.a_second_offset = H;
-    gu.n_proj = 2;
-    gu.out_f32 = gu_f32;
-    MOE_CUDA(launch_grouped_gemm(Kind::Proj, 128, m13, mx, gu, num_sms(), st), "gate/up projection launch");
-    MOE_CUDA(launch_swiglu_quant(gu_f32, T, H, hq, hs_t, num_sms(), st), "SwiGLU quantise launch");
+    gu.hq = hq;
+    gu.hs_t = hs_t;
+    MOE_CUDA(launch_grouped_gemm(Kind::GateUpWide, 128, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
     GemmArgs dn{};
     dn.G = 1;
     dn.num_kb = H / 128;
@@ -661,8 +671,13 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     dn.w_scale = w2_s;
     dn.a_rows_per_group = d;
     dn.out = static_cast<__nv_bfloat16 *>(y);
-    MOE_CUDA(launch_grouped_gemm(Kind::Down, 128, m2, mh, dn, num_sms(), st), "down GEMM launch");
-    t_launches = 4;
+    if (down_wide) {
+        dn.num_mb = d / 256;
+        MOE_CUDA(launch_grouped_gemm(Kind::DownWide, 128, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    } else {
+        MOE_CUDA(launch_grouped_gemm(Kind::Down, 128, m2, mh, dn, num_sms(), st), "down GEMM launch");
+    }
+    t_launches = 3;
     return MOE_OK;
 }
 

@@ -14,10 +14,12 @@ template <Kind KIND, int BN>
 static cudaError_t launch_kind(const CUtensorMap &map_a, const ActMaps &map_b, const GemmArgs &args,
                                int grid, cudaStream_t stream) {
     constexpr size_t smem = gemm_smem_bytes<KIND, BN>();
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    void (*kernel)(const CUtensorMap, const ActMaps, const GemmArgs);
+    if constexpr (KindCfg<KIND, BN>::kWide) kernel = grouped_gemm_wide_kernel<KIND, BN>;
+    else kernel = grouped_gemm_kernel<KIND, BN>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<KIND, BN><<<grid, KindCfg<KIND, BN>::kThreads, smem, stream>>>(map_a, map_b, args);
+    kernel<<<grid, KindCfg<KIND, BN>::kThreads, smem, stream>>>(map_a, map_b, args);
     return cudaGetLastError();
 }
 
@@ -26,7 +28,8 @@ static cudaError_t launch_kind(const CUtensorMap &map_a, const ActMaps &map_b, c
 template <Kind KIND>
 static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const ActMaps &map_b, const GemmArgs &args,
                              int grid, cudaStream_t stream) {
-    constexpr bool kTokenMajor = (KIND == Kind::Proj || KIND == Kind::Down);
+    constexpr bool kTokenMajor = (KIND == Kind::Proj || KIND == Kind::Down || KIND == Kind::GateUpWide ||
+                                  KIND == Kind::DownWide);
     switch (bn) {
         case 32:
             if constexpr (!kTokenMajor) return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
@@ -50,6 +53,8 @@ cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, con
         case Kind::Router: return launch_bn<Kind::Router>(bn, map_a, map_b, args, grid, stream);
         case Kind::Proj: return launch_bn<Kind::Proj>(bn, map_a, map_b, args, grid, stream);
         case Kind::DownPair: return launch_bn<Kind::DownPair>(bn, map_a, map_b, args, grid, stream);
+        case Kind::GateUpWide: return launch_bn<Kind::GateUpWide>(bn, map_a, map_b, args, grid, stream);
+        case Kind::DownWide: return launch_bn<Kind::DownWide>(bn, map_a, map_b, args, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

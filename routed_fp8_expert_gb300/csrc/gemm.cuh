@@ -52,7 +52,10 @@ namespace moe {
 //         (like GateUp's two tiles): twice the weight bytes per K block for the
 //         same per-K-block fixed costs; used for decode-sized tiles.
 // Router: bf16 router logits.
-enum class Kind { GateUp, Down, Router, Proj, DownPair };
+// GateUpWide: token-major, the gate and up blocks of the same 128 features as one
+//         N = 256 item, with the fused SiLU*mul and h quantisation.
+// DownWide: token-major down projection with two adjacent 128-row blocks (N = 256).
+enum class Kind { GateUp, Down, Router, Proj, DownPair, GateUpWide, DownWide };
 
 constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
@@ -68,12 +71,14 @@ constexpr int pow2_at_least(int v, int lo) { return v <= lo ? lo : 2 * pow2_at_l
 
 // Per-kind, per-tile-width configuration. BN = tokens per tile (MMA N upper bound).
 template <Kind K, int BN> struct KindCfg {
-    // weight tiles per K block: gate and up (GateUp) or two row blocks (DownPair)
-    static constexpr int kATiles = (K == Kind::GateUp || K == Kind::DownPair) ? 2 : 1;
+    // token-major with 256 weight rows per item (two 128-row tiles per K block)
+    static constexpr bool kWide = (K == Kind::GateUpWide || K == Kind::DownWide);
+    // weight tiles per K block: gate and up, or two row blocks
+    static constexpr int kATiles = (K == Kind::GateUp || K == Kind::DownPair || kWide) ? 2 : 1;
     static constexpr bool kPromote = (K != Kind::Router);         // per-128-K fp32 promotion
     static constexpr bool kBf16 = (K == Kind::Router);
     // token-major: tokens on the TMEM lanes (M = 128), weight rows on the columns
-    static constexpr bool kTM = (K == Kind::Proj || K == Kind::Down);
+    static constexpr bool kTM = (K == Kind::Proj || K == Kind::Down || kWide);
     // K blocks per stage: the single-tile FP8 kinds load two consecutive K blocks
     // per TMA request (3D maps with a K-block dimension), halving the requests
     static constexpr int kKPS = (K == Kind::Proj || K == Kind::Down) ? 2 : 1;
@@ -81,7 +86,7 @@ template <Kind K, int BN> struct KindCfg {
     static constexpr int kAStageBytes = kKPS * kATiles * kATileBytes;   // weight part of a stage
     static constexpr int kStageBytes = kAStageBytes + kKPS * kBTileBytes;
     static constexpr int kStages = (kStageBudget / kStageBytes) > 12 ? 12 : (kStageBudget / kStageBytes);
-    static constexpr int kPartCols = kTM ? kBM : kATiles * BN;    // one TMEM partial buffer
+    static constexpr int kPartCols = kATiles * (kTM ? kBM : BN);  // one TMEM partial buffer
     // partial buffers in flight between the MMA issuer and the epilogue: as
     // many as TMEM holds, up to 4, so the MMAs run ahead of the promotion
     static constexpr int kNumPart = (512 / kPartCols) >= 4 ? 4 : (512 / kPartCols);
@@ -89,13 +94,17 @@ template <Kind K, int BN> struct KindCfg {
     // scale slots: their own ring, released by the epilogue, so operand stages
     // are released by the MMA alone and the producer keeps kStages ahead of it
     static constexpr int kScaleSlots = kPromote ? (kStages + kNumPart + 2) : 1;
-    // epilogue column groups: token columns (swap-AB) or weight rows (token-major)
-    static constexpr int kGroups = 2;
-    static constexpr int kHalfCols = (kTM ? kBM : BN) / kGroups;  // columns per column group
+    // epilogue column groups: token columns (swap-AB) or weight rows (token-major);
+    // four for the 256-row items, so that each thread holds 64 accumulators
+    static constexpr int kGroups = kWide ? 4 : 2;
+    static constexpr int kHalfCols = kWide ? 64 : (kTM ? kBM : BN) / kGroups;  // accumulators per thread
     static constexpr int kChunks = kHalfCols / 16;
     static constexpr int kEpiWarps = 4 * kGroups;                 // one warp per TMEM lane quarter and group
-    static constexpr int kScaleWarp = 2 + kEpiWarps;               // copies the K blocks' scales
-    static constexpr int kThreads = 64 + 32 * kEpiWarps + (kPromote ? 32 : 0);
+    // the K blocks' scales are copied by a warp of their own, or, in the 19-warp
+    // wide kinds, by the producer warp (18 warps leave 112 registers a thread)
+    static constexpr bool kScaleWarpOwn = kPromote && !kWide;
+    static constexpr int kScaleWarp = 2 + kEpiWarps;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps + (kScaleWarpOwn ? 32 : 0);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
     static_assert(!kTM || BN == 128, "token-major tiles hold 128 tokens (the MMA M dimension)");
     static_assert(kStages * kKPS >= 4 && kStages >= 2, "pipeline depth");
@@ -220,18 +229,19 @@ template <Kind KIND, int BN> struct SmemLayout {
     static constexpr size_t kRs = kTp + kMaxGroups * 4;
     static constexpr int kScaleStride = BN + 4;                                // floats per stage: BN act + 2 weight
     static constexpr size_t kScale = kRs + kMaxGroups * 4;                     // [kScaleSlots][kScaleStride]
-    static constexpr size_t kCs = kScale + C::kScaleSlots * kScaleStride * 4;  // [warps][2][kATiles][HC]
-    static constexpr size_t kAmax = kCs + C::kEpiWarps * 2 * C::kATiles * C::kHalfCols * 4;  // [groups][2][4][HC]
+    static constexpr size_t kCs = kScale + C::kScaleSlots * kScaleStride * 4;  // [warps][2][kATiles][HC], swap-AB
+    static constexpr size_t kAmax = kCs + (C::kTM ? 0 : C::kEpiWarps * 2 * C::kATiles * C::kHalfCols * 4);  // [groups][2][4][HC]
     static constexpr size_t kEnd = kAmax + C::kGroups * 2 * 4 * C::kHalfCols * 4;
     static constexpr size_t kLaunchBytes = kEnd + 1024;  // + alignment slack of the dynamic base
     static_assert(kBars % 1024 == 0 && kScale % 16 == 0 && kCs % 16 == 0, "alignment");
     static_assert(kLaunchBytes <= 232448, "shared memory budget");
 };
 
+// The kernel body; map_a and map_b are the kernels' grid-constant parameters,
+// whose addresses the TMA instructions take.
 template <Kind KIND, int BN>
-__global__ void __launch_bounds__(KindCfg<KIND, BN>::kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ ActMaps map_b,
-                    const GemmArgs args) {
+__device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, const ActMaps &map_b,
+                                                  const GemmArgs &args) {
     using C = KindCfg<KIND, BN>;
     using L = SmemLayout<KIND, BN>;
     constexpr int kStageBytes = C::kStageBytes;
@@ -289,7 +299,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         for (int b = 0; b < 2 * C::kGroups; ++b) mbar_init(smem_u32(&amax_bar[b]), 4);
         for (int b = 0; b < kItemQ; ++b) {
             mbar_init(smem_u32(&item_full[b]), 1);
-            mbar_init(smem_u32(&item_empty[b]), 1 + kEpi + (C::kPromote ? 1 : 0));
+            mbar_init(smem_u32(&item_empty[b]), 1 + kEpi + (C::kScaleWarpOwn ? 1 : 0));
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -313,6 +323,36 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         return it;
     };
 
+    // The weight-scale rows [num_kb] of an item's block(s).
+    auto weight_scale_rows = [&](const Item &I, const float *&ws0, const float *&ws1) {
+        ws1 = nullptr;
+        if constexpr (KIND == Kind::Proj) {
+            ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + I.proj) * args.num_mb + I.mb) * args.num_kb;
+        } else if constexpr (KIND == Kind::GateUp || KIND == Kind::GateUpWide) {
+            ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
+            ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
+        } else if constexpr (KIND == Kind::DownPair || KIND == Kind::DownWide) {
+            // row blocks 2mb and 2mb+1 of the group's [2 * num_mb][num_kb] scale grid
+            ws0 = args.w_scale + (static_cast<size_t>(I.g) * 2 * args.num_mb + 2 * I.mb) * args.num_kb;
+            ws1 = ws0 + args.num_kb;
+        } else {
+            ws0 = args.w_scale + (static_cast<size_t>(I.g) * args.num_mb + I.mb) * args.num_kb;
+        }
+    };
+    // K block kb's scales into slot `slot`: the activation scales of the tile's
+    // tokens and the weight scale(s) of the block (cp.async, 4 bytes per lane and
+    // copy); the slot's full barrier counts one arrival per lane.
+    auto copy_scales = [&](const Item &I, int kb, int slot, const float *ws0, const float *ws1) {
+        const uint32_t sdst = smem_u32(s_scale + slot * L::kScaleStride);
+        const float *src = args.act_scale_t + static_cast<size_t>(kb) * args.total_rows + I.row0;
+        for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
+        if (lane == 0) {
+            cp_async_4(sdst + 4 * BN, ws0 + kb);
+            if constexpr (C::kATiles == 2) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
+        }
+        cp_async_arrive_noinc(smem_u32(&sfull[slot]));
+    };
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // lane 0 fetches items and issues the TMA tile loads
@@ -328,6 +368,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         int q = 0;
         uint32_t qphase = 0;
         int next_static = blockIdx.x;
+        int sslot = 0;                 // wide kinds: the producer also copies the scales
+        uint32_t sphase = 0;
         while (true) {
             int it = 0, got = 1;
             if (lane == 0) {
@@ -361,10 +403,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             if constexpr (KIND == Kind::Router) {
                 arow0 = I.mb * kBM;
             } else {
-                constexpr int kRowsPerBlock = (KIND == Kind::DownPair) ? 2 * kBM : kBM;
+                constexpr int kRowsPerBlock = (KIND == Kind::DownPair || KIND == Kind::DownWide) ? 2 * kBM : kBM;
                 arow0 = I.g * args.a_rows_per_group + I.mb * kRowsPerBlock;
                 if constexpr (KIND == Kind::Proj) arow0 += I.proj * args.a_second_offset;
             }
+            const float *ws0 = nullptr, *ws1 = nullptr;
+            if constexpr (C::kWide) weight_scale_rows(I, ws0, ws1);
             bool ok = true;
             for (int kb = kb0; kb < kb1; kb += C::kKPS) {
                 int w = 1;
@@ -385,7 +429,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                         tma_load_3d(sbase + C::kAStageBytes, &map_b.box[box_i], fb, 0, I.row0, kb, pol_x);
                     } else {
                         const int kx = kb * kKbElems;
-                        if constexpr (KIND == Kind::GateUp)
+                        if constexpr (KIND == Kind::GateUp || KIND == Kind::GateUpWide)
                             tma_load_3d(sbase, &map_a, fb, kx, I.mb * kBM, 2 * I.g, pol_w);
                         else
                             tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
@@ -395,9 +439,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                if constexpr (C::kWide) {
+                    if (lane == 0) w = mbar_wait(smem_u32(&sempty[sslot]), sphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (!w) { ok = false; break; }
+                    copy_scales(I, kb, sslot, ws0, ws1);
+                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
+                }
             }
             if (!ok) break;
         }
+        if constexpr (C::kWide) cp_async_wait_all();   // the scale copies must land before the CTA may exit
         // every issued copy must land before the CTA may exit
         if (lane == 0)
             for (int s = 0; s < C::kStages; ++s)
@@ -421,7 +473,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 kb_range(args, I, kb0, kb1);
                 // swap-AB: M = 128 weight rows, N = the tile's tokens rounded up to 16;
                 // token-major: M = 128 tokens, N = 128 weight rows
-                const int n_mma = C::kTM ? kBM : ((I.n + 15) & ~15);
+                const int n_mma = C::kTM ? C::kPartCols : ((I.n + 15) & ~15);
                 const uint32_t idesc = idesc_make(kFmt, kFmt, kBM, n_mma);
                 // bytes of one K block's activation sub-tile inside a K-pair box
                 const uint32_t b_kb_bytes = kActBoxHeights[act_box_index<C::kTM>(I.n)] * kKBytes;
@@ -450,7 +502,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                             if constexpr (C::kBf16) mma_bf16(dcol, adesc, bdesc, idesc, acc);
                             else if constexpr (C::kTM) mma_f8(dcol, bdesc, adesc, idesc, acc);
                             else mma_f8(dcol, adesc, bdesc, idesc, acc);
-                            if constexpr (C::kATiles == 2)
+                            if constexpr (C::kATiles == 2 && !C::kTM)
                                 mma_f8(dcol + BN, sdesc_sw128(abase + kATileBytes + k * 32), bdesc, idesc, acc);
                         }
                         if (C::kPromote || kbh == kb1 - 1) {
@@ -467,12 +519,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             mma_commit(smem_u32(mma_done));
             mbar_wait_drain(smem_u32(mma_done), 0, args.err);
         }
-    } else if (C::kPromote && warp == C::kScaleWarp) {
+    } else if (C::kScaleWarpOwn && warp == C::kScaleWarp) {
         // ------------------------------------------------------------ scale copier
-        // per K block: the activation scales of the tile's tokens and the weight
-        // scale(s) of the block, into the next scale slot (cp.async, 4 bytes per
-        // lane and copy); runs beside the producer so the TMA issue never waits
-        // on these copies
+        // per K block, the scales into the next scale slot; runs beside the producer
+        // so the TMA issue never waits on these copies
         int sslot = 0;
         uint32_t sphase = 0;
         int q = 0;
@@ -485,32 +535,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             if (it < 0 || it >= n_items) break;
             Item I;
             if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
-            const float *ws0, *ws1 = nullptr;
-            if constexpr (KIND == Kind::Proj) {
-                ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + I.proj) * args.num_mb + I.mb) * args.num_kb;
-            } else if constexpr (KIND == Kind::GateUp) {
-                ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
-                ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
-            } else if constexpr (KIND == Kind::DownPair) {
-                // row blocks 2mb and 2mb+1 of the group's [2 * num_mb][num_kb] scale grid
-                ws0 = args.w_scale + (static_cast<size_t>(I.g) * 2 * args.num_mb + 2 * I.mb) * args.num_kb;
-                ws1 = ws0 + args.num_kb;
-            } else {
-                ws0 = args.w_scale + (static_cast<size_t>(I.g) * args.num_mb + I.mb) * args.num_kb;
-            }
+            const float *ws0, *ws1;
+            weight_scale_rows(I, ws0, ws1);
             for (int kb = 0; kb < args.num_kb; ++kb) {
                 int w = 1;
                 if (lane == 0) w = mbar_wait(smem_u32(&sempty[sslot]), sphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w) { ok = false; break; }
-                const uint32_t sdst = smem_u32(s_scale + sslot * L::kScaleStride);
-                const float *src = args.act_scale_t + static_cast<size_t>(kb) * args.total_rows + I.row0;
-                for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
-                if (lane == 0) {
-                    cp_async_4(sdst + 4 * BN, ws0 + kb);
-                    if constexpr (C::kATiles == 2) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
-                }
-                cp_async_arrive_noinc(smem_u32(&sfull[sslot]));
+                copy_scales(I, kb, sslot, ws0, ws1);
                 if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
             }
         }
@@ -538,7 +570,112 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             Item I;
             if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
             const int n_my = max(0, min(HC, I.n - col_base));
-            if constexpr (C::kTM) {
+            if constexpr (C::kWide) {
+                // token-major, 256 weight rows: thread = token row r; its 64 accumulators are
+                //   GateUpWide: gate [0, 32) and up [32, 64) of features 32*grp .. 32*grp+31
+                //   DownWide:   the 64 output rows 64*grp .. of the item's 256
+                const int r = quad * 32 + lane;
+                float acc[HC];
+#pragma unroll
+                for (int j = 0; j < HC; ++j) acc[j] = 0.f;
+                // TMEM column of 16-column chunk c (0..3) inside a partial buffer
+                auto chunk_col = [&](int c) -> uint32_t {
+                    if constexpr (KIND == Kind::GateUpWide) return (c >> 1) * kBM + grp * 32 + (c & 1) * 16;
+                    else return grp * 64 + c * 16;
+                };
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&pfull[pbuf]), pphase, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t tpart = t_lane + pbuf * C::kPartCols;
+                    float p[16];
+                    tmem_ld16(tpart + chunk_col(0), p);
+                    if (!mbar_wait(smem_u32(&sfull[sslot]), sphase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) {
+                        tmem_wait_ld();
+                        ok = false;
+                        break;
+                    }
+                    // this token's scales for the K block: s_w[block, kb] * s_x[row r, kb]
+                    // (rows beyond the tile's end compute on stale slot entries, never stored)
+                    const float *sc = s_scale + sslot * L::kScaleStride;
+                    const float sx = sc[r];
+                    float s_lo, s_hi;
+                    if constexpr (KIND == Kind::GateUpWide) {
+                        s_lo = sc[BN] * sx;       // gate block
+                        s_hi = sc[BN + 1] * sx;   // up block
+                    } else {
+                        s_lo = sc[BN + (grp >> 1)] * sx;
+                        s_hi = s_lo;
+                    }
+                    // one 16-column chunk in flight at a time (the 64 accumulators and
+                    // 16 partials fill the registers of the 19-warp CTA)
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        if (c > 0) tmem_ld16(tpart + chunk_col(c), p);
+                        tmem_wait_ld();
+                        const float s_c = (c < 2) ? s_lo : s_hi;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s_c, p[i], acc[c * 16 + i]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&pempty[pbuf]));
+                        mbar_arrive(smem_u32(&sempty[sslot]));
+                    }
+                    if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
+                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
+                }
+                if (!ok) break;
+                const size_t row = static_cast<size_t>(I.row0 + r);
+                if constexpr (KIND == Kind::GateUpWide) {
+                    // h = silu(g) * u for the token's 32 features, then the 1x128 amax
+                    // over the block's 128 features, held by the four column-group
+                    // warps of this lane quarter: exchanged through shared memory
+                    const int H = args.num_mb * kBM;
+                    const int buf = item_count & 1;
+                    const uint32_t ab = smem_u32(&amax_bar[quad * 2 + buf]);
+                    float *xch = s_amax + buf * 4 * kBM;   // [group][token row]
+                    float am = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        acc[j] = silu_f(acc[j]) * acc[32 + j];
+                        am = fmaxf(am, fabsf(acc[j]));
+                    }
+                    xch[grp * kBM + r] = am;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ab);
+                    if (!mbar_wait(ab, (item_count >> 1) & 1, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
+                    if (r < I.n) {
+                        const float amax = fmaxf(fmaxf(xch[r], xch[kBM + r]), fmaxf(xch[2 * kBM + r], xch[3 * kBM + r]));
+                        const float sq = amax / 448.0f;
+                        // codes in feature order, four to a word (the first in the low byte);
+                        // an all-zero group has scale 0 and codes 0
+                        uint32_t w[8];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const uint32_t lo = e4m3x2(acc[4 * v] / sq, acc[4 * v + 1] / sq);
+                            const uint32_t hi = e4m3x2(acc[4 * v + 2] / sq, acc[4 * v + 3] / sq);
+                            w[v] = (amax == 0.f) ? 0u : (lo | (hi << 16));
+                        }
+                        uint4 *h4 = reinterpret_cast<uint4 *>(args.hq + row * H + I.mb * kBM + grp * 32);
+                        h4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        h4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        if (grp == 0) args.hs_t[static_cast<size_t>(I.mb) * args.total_rows + row] = sq;
+                    }
+                } else if (r < I.n) {
+                    const int nout = args.num_mb * 2 * kBM;   // output features per row
+                    uint4 *o4 = reinterpret_cast<uint4 *>(args.out + row * nout + I.mb * 2 * kBM + grp * 64);
+#pragma unroll
+                    for (int v = 0; v < HC / 8; ++v) {
+                        uint4 w;
+                        w.x = bf16x2_bits(acc[8 * v + 0], acc[8 * v + 1]);
+                        w.y = bf16x2_bits(acc[8 * v + 2], acc[8 * v + 3]);
+                        w.z = bf16x2_bits(acc[8 * v + 4], acc[8 * v + 5]);
+                        w.w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
+                        o4[v] = w;
+                    }
+                }
+            } else if constexpr (C::kTM) {
                 // token-major: this thread's TMEM lane is token row r of the tile, its
                 // columns the weight rows [col_base, col_base + 64) of block mb
                 const int r = quad * 32 + lane;
@@ -760,6 +897,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc<C::kTmemCols>(tmem_base);
+}
+
+template <Kind KIND, int BN>
+__global__ void __launch_bounds__(KindCfg<KIND, BN>::kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ ActMaps map_b,
+                    const GemmArgs args) {
+    grouped_gemm_body<KIND, BN>(map_a, map_b, args);
+}
+
+// The 18-warp CTAs of the 256-row token-major kinds: 112 registers per thread
+// (18 x 32 x 112 = 64,512 of the SM's 65,536) for the epilogue's 64 accumulators
+// and 16 partials; the launch-bounds heuristic alone would allow 96.
+template <Kind KIND, int BN>
+__global__ void __maxnreg__(96)
+grouped_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ ActMaps map_b,
+                         const GemmArgs args) {
+    grouped_gemm_body<KIND, BN>(map_a, map_b, args);
 }
 
 template <Kind KIND, int BN>
