@@ -383,7 +383,7 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
     if NCU_TRAFFIC and NCU_TRAFFIC.get("src") == kernel_src_hash() and expert_bn_is_decode(shape):
         traffic_val = NCU_TRAFFIC["ratio"] * gu_bytes
     gu_kernel = ("grouped_gemm_kernel<GateUp, 32>" if expert_bn_is_decode(shape) else
-                 "grouped_gemm_kernel<Proj, 128> + swiglu_quant_kernel")
+                 "grouped_gemm_wide_kernel<GateUpWide, 128>")
     layer_weight_bytes = touched * (3 * H * d + 3 * (H // 128) * (d // 128) * 4) + E * d * 2
     flops = T * (2 * E * d) + (T * k + T * Sh) * 6 * d * H
     ms_step = ms_total / args.steps

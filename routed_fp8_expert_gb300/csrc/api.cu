@@ -144,7 +144,6 @@ struct LayerWs {
     uint8_t *hq;
     float *hs_t;
     __nv_bfloat16 *o;
-    float *gu;          // [2][R][H] fp32 gate and up projections (beyond the decode regime)
     size_t bytes;
 };
 
@@ -175,7 +174,6 @@ LayerWs carve_layer(const moe_cfg_t &c, int T, void *base) {
     w.hq = cv.take<uint8_t>(R * c.H);
     w.hs_t = cv.take<float>(R * (c.H / 128) * 4);
     w.o = cv.take<__nv_bfloat16>(R * c.d * 2);
-    w.gu = cv.take<float>(2 * R * c.H * 4);
     w.bytes = align_up(cv.off, 1024);
     return w;
 }
@@ -319,7 +317,6 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     gu.act_scale_t = sx_perm;
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * c.H;
-    gu.a_second_offset = c.H;
     if (decode_regime(c, T)) {
         // fused gate/up + SiLU*mul + h quantisation; static item order (uniform
         // items, one token tile per routed expert)
@@ -374,7 +371,6 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
         // weights per K block and request)
         MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
         dn.num_mb = c.d / 256;
-        dn.a_second_offset = kBM;
         MOE_CUDA(launch_grouped_gemm(Kind::DownPair, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     } else if ((c.d / 128) % 2 == 0) {
         // 128-token tiles, token-major, two 128-row blocks per item (N = 256)
@@ -609,7 +605,6 @@ size_t dense_swiglu_workspace_bytes(int d, int H, int T) {
     cv.take<float>(Tz * (d / 128) * 4);
     cv.take<uint8_t>(Tz * H);
     cv.take<float>(Tz * (H / 128) * 4);
-    cv.take<float>(2 * Tz * H * 4);
     return align_up(cv.off, 1024);
 }
 
@@ -633,7 +628,6 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     float *sx_t = cv.take<float>(Tz * (d / 128) * 4);
     uint8_t *hq = cv.take<uint8_t>(Tz * H);
     float *hs_t = cv.take<float>(Tz * (H / 128) * 4);
-    float *gu_f32 = cv.take<float>(2 * Tz * H * 4);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     MOE_CUDA(launch_quant(x, true, T, d, xq, sx_t, true, num_sms(), st), "quantise launch");
     CUtensorMap m13, m2;
@@ -657,7 +651,6 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s, cons
     gu.act_scale_t = sx_t;
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * H;
-    gu.a_second_offset = H;
     gu.hq = hq;
     gu.hs_t = hs_t;
     MOE_CUDA(launch_grouped_gemm(Kind::GateUpWide, 128, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");

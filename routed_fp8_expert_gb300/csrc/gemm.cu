@@ -28,8 +28,7 @@ static cudaError_t launch_kind(const CUtensorMap &map_a, const ActMaps &map_b, c
 template <Kind KIND>
 static cudaError_t launch_bn(int bn, const CUtensorMap &map_a, const ActMaps &map_b, const GemmArgs &args,
                              int grid, cudaStream_t stream) {
-    constexpr bool kTokenMajor = (KIND == Kind::Proj || KIND == Kind::Down || KIND == Kind::GateUpWide ||
-                                  KIND == Kind::DownWide);
+    constexpr bool kTokenMajor = (KIND == Kind::Down || KIND == Kind::GateUpWide || KIND == Kind::DownWide);
     switch (bn) {
         case 32:
             if constexpr (!kTokenMajor) return launch_kind<KIND, 32>(map_a, map_b, args, grid, stream);
@@ -51,7 +50,6 @@ cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, con
         case Kind::GateUp: return launch_bn<Kind::GateUp>(bn, map_a, map_b, args, grid, stream);
         case Kind::Down: return launch_bn<Kind::Down>(bn, map_a, map_b, args, grid, stream);
         case Kind::Router: return launch_bn<Kind::Router>(bn, map_a, map_b, args, grid, stream);
-        case Kind::Proj: return launch_bn<Kind::Proj>(bn, map_a, map_b, args, grid, stream);
         case Kind::DownPair: return launch_bn<Kind::DownPair>(bn, map_a, map_b, args, grid, stream);
         case Kind::GateUpWide: return launch_bn<Kind::GateUpWide>(bn, map_a, map_b, args, grid, stream);
         case Kind::DownWide: return launch_bn<Kind::DownWide>(bn, map_a, map_b, args, grid, stream);

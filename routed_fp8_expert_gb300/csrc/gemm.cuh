@@ -6,7 +6,7 @@
 //   swap-AB (decode-sized tiles: GateUp, DownPair, Router): the block's weight
 //     rows are the MMA M dimension (TMEM lanes) and the tile's tokens the N
 //     dimension (TMEM columns), so a handful of tokens costs an N=16 MMA;
-//   token-major (128-token tiles: Proj, Down): the tile's 128 tokens are M and
+//   token-major (128-token tiles: GateUpWide, DownWide, Down): the tile's 128 tokens are M and
 //     the block's 128 weight rows N. Each epilogue thread then owns one token,
 //     and the per-K-block scale s_w[mb,kb] * s_x[token,kb] is one scalar per
 //     thread instead of one value per column.
@@ -44,10 +44,9 @@
 namespace moe {
 
 // GateUp: gate and up projections of one weight block, fused SiLU*mul and h quantisation.
-// Proj:   one projection (gate or up) per item, token-major, fp32 output; SiLU*mul
-//         and h quantisation follow in a separate kernel. Items carry half the
-//         weight tiles of GateUp, so 128-token tiles fit the epilogue's registers.
-// Down:   down projection, token-major, bf16 output.
+// Down:   token-major down projection with one 128-row block per item, bf16
+//         output (the wide-tile down projection when the output has an odd
+//         number of 128-row blocks).
 // DownPair: down projection with two adjacent 128-row weight blocks per item
 //         (like GateUp's two tiles): twice the weight bytes per K block for the
 //         same per-K-block fixed costs; used for decode-sized tiles.
@@ -55,7 +54,7 @@ namespace moe {
 // GateUpWide: token-major, the gate and up blocks of the same 128 features as one
 //         N = 256 item, with the fused SiLU*mul and h quantisation.
 // DownWide: token-major down projection with two adjacent 128-row blocks (N = 256).
-enum class Kind { GateUp, Down, Router, Proj, DownPair, GateUpWide, DownWide };
+enum class Kind { GateUp, Down, Router, DownPair, GateUpWide, DownWide };
 
 constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
@@ -78,10 +77,10 @@ template <Kind K, int BN> struct KindCfg {
     static constexpr bool kPromote = (K != Kind::Router);         // per-128-K fp32 promotion
     static constexpr bool kBf16 = (K == Kind::Router);
     // token-major: tokens on the TMEM lanes (M = 128), weight rows on the columns
-    static constexpr bool kTM = (K == Kind::Proj || K == Kind::Down || kWide);
-    // K blocks per stage: the single-tile FP8 kinds load two consecutive K blocks
-    // per TMA request (3D maps with a K-block dimension), halving the requests
-    static constexpr int kKPS = (K == Kind::Proj || K == Kind::Down) ? 2 : 1;
+    static constexpr bool kTM = (K == Kind::Down || kWide);
+    // K blocks per stage: the single-tile token-major kind loads two consecutive K
+    // blocks per TMA request (3D maps with a K-block dimension)
+    static constexpr int kKPS = (K == Kind::Down) ? 2 : 1;
     static constexpr int kBTileBytes = BN * kKBytes;
     static constexpr int kAStageBytes = kKPS * kATiles * kATileBytes;   // weight part of a stage
     static constexpr int kStageBytes = kAStageBytes + kKPS * kBTileBytes;
@@ -122,12 +121,9 @@ struct GemmArgs {
     const float *act_scale_t; // [num_kb][total_rows]  (FP8 kinds)
     const float *w_scale;     // GateUp: [G][2][num_mb][num_kb]; Down: [G][num_mb][num_kb]
     int a_rows_per_group;     // weight rows of one group in the A tensor map (GateUp: 2*H, Down: d_out)
-    int a_second_offset;      // GateUp: row offset of up_proj inside a group (H)
     uint8_t *hq;              // GateUp: [total_rows][num_mb*128]
     float *hs_t;              // GateUp: [num_mb][total_rows]
     __nv_bfloat16 *out;       // Down: [total_rows][num_mb*128]
-    float *out_f32;           // Proj: [2][total_rows][num_mb*128] gate (0) and up (1) projections
-    int n_proj;               // Proj: 2 (items per weight block: gate, up); 1 otherwise
     float *logits;            // Router: [k_splits][total_rows][n_valid] partial logits
     int n_valid;              // Router: valid weight rows (experts)
     int k_splits;             // Router: K range split into this many partial sums (>= 1)
@@ -137,17 +133,15 @@ struct GemmArgs {
 
 struct Item {
     int g, mb, row0, n, ks;
-    int proj;     // Proj: 0 gate, 1 up
     int ntiles;   // token tiles of the item's group (tiles sharing its weight block)
 };
 
-// Items of a group are ordered (weight block, projection, token tile) with the
-// token tile fastest, so the tiles that share a weight block are adjacent.
+// Items of a group are ordered (weight block, token tile) with the token tile
+// fastest, so the tiles that share a weight block are adjacent.
 template <int BN>
 __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int *s_tp,
                                             const int *s_rs, Item &o) {
-    const int nproj = a.n_proj > 1 ? a.n_proj : 1;
-    const int nblk = a.num_mb * nproj;   // weight blocks x projections
+    const int nblk = a.num_mb;   // weight blocks per group
     int mbx;
     if (a.single_rows >= 0) {
         // items = (block, token tile, K split) with the split fastest
@@ -180,14 +174,13 @@ __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int
         o.n = min(BN, s_rs[g + 1] - o.row0);
         o.ntiles = nt_g;
     }
-    o.mb = mbx / nproj;
-    o.proj = mbx - o.mb * nproj;
+    o.mb = mbx;
     return o.n > 0 && o.mb < a.num_mb;
 }
 
 template <int BN>
 __device__ __forceinline__ int total_items(const GemmArgs &a, const int *s_tp) {
-    const int nblk = a.num_mb * (a.n_proj > 1 ? a.n_proj : 1);
+    const int nblk = a.num_mb;
     if (a.single_rows >= 0)
         return nblk * ((a.single_rows + BN - 1) / BN) * (a.k_splits > 0 ? a.k_splits : 1);
     return nblk * s_tp[a.G];
@@ -265,7 +258,8 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     uint64_t *sfull = item_empty + kItemQ;               // [kScaleSlots]
     uint64_t *sempty = sfull + C::kScaleSlots;           // [kScaleSlots]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *abort_word = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    const uint32_t abort_flag = smem_u32(smem + L::kMisc + 4);   // shared address of the abort word
     volatile int *s_items = reinterpret_cast<volatile int *>(smem + L::kItems);
     int *s_tp = reinterpret_cast<int *>(smem + L::kTp);
     int *s_rs = reinterpret_cast<int *>(smem + L::kRs);
@@ -301,7 +295,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             mbar_init(smem_u32(&item_full[b]), 1);
             mbar_init(smem_u32(&item_empty[b]), 1 + kEpi + (C::kScaleWarpOwn ? 1 : 0));
         }
-        *abort_flag = 0;
+        *abort_word = 0;
         fence_barrier_init();
         tma_prefetch_desc(&map_a);
         for (int i = 0; i < kActBoxes; ++i) tma_prefetch_desc(&map_b.box[i]);
@@ -326,9 +320,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     // The weight-scale rows [num_kb] of an item's block(s).
     auto weight_scale_rows = [&](const Item &I, const float *&ws0, const float *&ws1) {
         ws1 = nullptr;
-        if constexpr (KIND == Kind::Proj) {
-            ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + I.proj) * args.num_mb + I.mb) * args.num_kb;
-        } else if constexpr (KIND == Kind::GateUp || KIND == Kind::GateUpWide) {
+        if constexpr (KIND == Kind::GateUp || KIND == Kind::GateUpWide) {
             ws0 = args.w_scale + (static_cast<size_t>(I.g * 2 + 0) * args.num_mb + I.mb) * args.num_kb;
             ws1 = args.w_scale + (static_cast<size_t>(I.g * 2 + 1) * args.num_mb + I.mb) * args.num_kb;
         } else if constexpr (KIND == Kind::DownPair || KIND == Kind::DownWide) {
@@ -405,7 +397,6 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             } else {
                 constexpr int kRowsPerBlock = (KIND == Kind::DownPair || KIND == Kind::DownWide) ? 2 * kBM : kBM;
                 arow0 = I.g * args.a_rows_per_group + I.mb * kRowsPerBlock;
-                if constexpr (KIND == Kind::Proj) arow0 += I.proj * args.a_second_offset;
             }
             const float *ws0 = nullptr, *ws1 = nullptr;
             if constexpr (C::kWide) weight_scale_rows(I, ws0, ws1);
@@ -561,6 +552,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         int q = 0;
         uint32_t qphase = 0;
         int item_count = 0;
+        uint32_t kb_done = 0;                // wide kinds: K blocks promoted so far (both rings)
         bool ok = true;
         while (ok) {
             int it = 0;
@@ -583,20 +575,19 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     if constexpr (KIND == Kind::GateUpWide) return (c >> 1) * kBM + grp * 32 + (c & 1) * 16;
                     else return grp * 64 + c * 16;
                 };
-                for (int kb = 0; kb < args.num_kb; ++kb) {
-                    if (!mbar_wait(smem_u32(&pfull[pbuf]), pphase, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t tpart = t_lane + pbuf * C::kPartCols;
-                    float p[16];
-                    tmem_ld16(tpart + chunk_col(0), p);
-                    if (!mbar_wait(smem_u32(&sfull[sslot]), sphase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) {
-                        tmem_wait_ld();
-                        ok = false;
-                        break;
-                    }
+                // the partial ring and the scale ring advance together, one entry per K
+                // block, so one counter gives both positions
+                static_assert((C::kNumPart & (C::kNumPart - 1)) == 0 && (C::kScaleSlots & (C::kScaleSlots - 1)) == 0,
+                              "ring sizes are powers of two");
+                for (int kb = 0; kb < args.num_kb; ++kb, ++kb_done) {
+                    const uint32_t pb = kb_done & (C::kNumPart - 1), pph = (kb_done / C::kNumPart) & 1;
+                    const uint32_t ss = kb_done & (C::kScaleSlots - 1), sph = (kb_done / C::kScaleSlots) & 1;
+                    // the scales first (copied well ahead, so this wait seldom blocks): no
+                    // TMEM load is in flight across it, which keeps the registers free
+                    if (!mbar_wait(smem_u32(&sfull[ss]), sph, abort_flag, args.err, ERR_WAIT_TMA_FULL)) { ok = false; break; }
                     // this token's scales for the K block: s_w[block, kb] * s_x[row r, kb]
                     // (rows beyond the tile's end compute on stale slot entries, never stored)
-                    const float *sc = s_scale + sslot * L::kScaleStride;
+                    const float *sc = s_scale + ss * L::kScaleStride;
                     const float sx = sc[r];
                     float s_lo, s_hi;
                     if constexpr (KIND == Kind::GateUpWide) {
@@ -606,11 +597,15 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                         s_lo = sc[BN + (grp >> 1)] * sx;
                         s_hi = s_lo;
                     }
+                    if (!mbar_wait(smem_u32(&pfull[pb]), pph, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t tpart = t_lane + pb * C::kPartCols;
+                    float p[16];
                     // one 16-column chunk in flight at a time (the 64 accumulators and
                     // 16 partials fill the registers of the 19-warp CTA)
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c) {
-                        if (c > 0) tmem_ld16(tpart + chunk_col(c), p);
+                        tmem_ld16(tpart + chunk_col(c), p);
                         tmem_wait_ld();
                         const float s_c = (c < 2) ? s_lo : s_hi;
 #pragma unroll
@@ -619,11 +614,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(smem_u32(&pempty[pbuf]));
-                        mbar_arrive(smem_u32(&sempty[sslot]));
+                        mbar_arrive(smem_u32(&pempty[pb]));
+                        mbar_arrive(smem_u32(&sempty[ss]));
                     }
-                    if (++pbuf == C::kNumPart) { pbuf = 0; pphase ^= 1; }
-                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
                 }
                 if (!ok) break;
                 const size_t row = static_cast<size_t>(I.row0 + r);
@@ -719,23 +712,15 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     const size_t row = static_cast<size_t>(I.row0 + r);
                     const int nout = args.num_mb * kBM;   // output features per row
                     const size_t col = static_cast<size_t>(I.mb) * kBM + col_base;
-                    if constexpr (KIND == Kind::Proj) {
-                        float4 *d4 = reinterpret_cast<float4 *>(
-                            args.out_f32 + (static_cast<size_t>(I.proj) * args.total_rows + row) * nout + col);
+                    uint4 *o4 = reinterpret_cast<uint4 *>(args.out + row * nout + col);
 #pragma unroll
-                        for (int v = 0; v < HC / 4; ++v)
-                            d4[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
-                    } else {
-                        uint4 *o4 = reinterpret_cast<uint4 *>(args.out + row * nout + col);
-#pragma unroll
-                        for (int v = 0; v < HC / 8; ++v) {
-                            uint4 w;
-                            w.x = bf16x2_bits(acc[8 * v + 0], acc[8 * v + 1]);
-                            w.y = bf16x2_bits(acc[8 * v + 2], acc[8 * v + 3]);
-                            w.z = bf16x2_bits(acc[8 * v + 4], acc[8 * v + 5]);
-                            w.w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
-                            o4[v] = w;
-                        }
+                    for (int v = 0; v < HC / 8; ++v) {
+                        uint4 w;
+                        w.x = bf16x2_bits(acc[8 * v + 0], acc[8 * v + 1]);
+                        w.y = bf16x2_bits(acc[8 * v + 2], acc[8 * v + 3]);
+                        w.z = bf16x2_bits(acc[8 * v + 4], acc[8 * v + 5]);
+                        w.w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
+                        o4[v] = w;
                     }
                 }
             } else if constexpr (C::kPromote) {

@@ -27,8 +27,6 @@ cudaError_t device_error_word(unsigned int **ptr);
 // Small kernels (kernels.cu).
 cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint8_t *q, float *s,
                          bool s_transposed, int num_sms, cudaStream_t stream);
-cudaError_t launch_swiglu_quant(const float *gu, int64_t rows, int H, uint8_t *hq, float *hs, int num_sms,
-                                cudaStream_t stream);
 cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream);
 cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *sx, int T, int k, int S, int E,

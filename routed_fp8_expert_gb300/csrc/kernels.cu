@@ -19,16 +19,6 @@ cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint
     return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu_quant(const float *gu, int64_t rows, int H, uint8_t *hq, float *hs, int num_sms,
-                                cudaStream_t stream) {
-    const int64_t groups = rows * (H / 128);
-    int64_t blocks = (groups + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
-    if (blocks > cap) blocks = cap;
-    swiglu_quant_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(gu, rows, H, hq, hs);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream) {
     const int threads = 64;   // 2 tokens per block: a 256-token batch spreads over 128 blocks

@@ -49,39 +49,6 @@ __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, in
     }
 }
 
-// ------------------------------------------------------------------ SwiGLU + quantise
-// h = silu(g) * u from the gate and up projections (fp32 [rows][H] each, up
-// following gate), then the 1x128 quantisation of h: one warp per 128-wide
-// group. hq [rows][H] e4m3; hs [H/128][rows] fp32 (K-block-major).
-__global__ void swiglu_quant_kernel(const float *__restrict__ gu, int64_t rows, int H, uint8_t *__restrict__ hq,
-                                    float *__restrict__ hs) {
-    const int lane = threadIdx.x & 31;
-    const int gpr = H / 128;
-    const int64_t n_groups = rows * gpr;
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const float *up = gu + rows * H;
-    for (int64_t gi = warp0; gi < n_groups; gi += nwarps) {
-        const int64_t r = gi / gpr;
-        const int g = static_cast<int>(gi - r * gpr);
-        const int64_t base = r * H + g * 128 + lane * 4;
-        const float4 a = *reinterpret_cast<const float4 *>(gu + base);
-        const float4 b = *reinterpret_cast<const float4 *>(up + base);
-        const float h[4] = {a.x / (1.0f + expf(-a.x)) * b.x, a.y / (1.0f + expf(-a.y)) * b.y,
-                            a.z / (1.0f + expf(-a.z)) * b.z, a.w / (1.0f + expf(-a.w)) * b.w};
-        unsigned m = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m = max(m, __float_as_uint(fabsf(h[i])));
-        const float amax = __uint_as_float(__reduce_max_sync(kFull, m));
-        const float sc = amax / 448.0f;
-        uint32_t packed = 0;
-        if (amax != 0.f)
-            packed = e4m3x2(h[0] / sc, h[1] / sc) | (static_cast<uint32_t>(e4m3x2(h[2] / sc, h[3] / sc)) << 16);
-        *reinterpret_cast<uint32_t *>(hq + base) = packed;
-        if (lane == 0) hs[static_cast<int64_t>(g) * rows + r] = sc;
-    }
-}
-
 // ------------------------------------------------------------------ top-k
 // One warp per token. The logit is the sum of the router GEMM's K-split
 // partials, added in split order; scores s = sigmoid(logit) in fp32; choice

@@ -85,18 +85,29 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // suspensions.
 constexpr uint32_t kWaitSleepNs = 200000;
 
-// Wait until the phase with the given parity has completed. Gives up when
-// *abort becomes non-zero (another role gave up) or after kWaitLimitNs, in
-// which case it raises *abort and records `err_bit`. Returns false on give-up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+__device__ __forceinline__ int ld_volatile_shared(uint32_t addr) {
+    int v;
+    asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_volatile_shared(uint32_t addr, int v) {
+    asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Wait until the phase with the given parity has completed. Gives up when the
+// shared abort word at `abort_addr` becomes non-zero (another role gave up) or
+// after kWaitLimitNs, in which case it raises the abort word and records
+// `err_bit`. Returns false on give-up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t abort_addr,
                                           unsigned int *err, uint32_t err_bit) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
-        if (*abort) return false;
+        if (ld_volatile_shared(abort_addr)) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
-            *abort = 1;
+            st_volatile_shared(abort_addr, 1);
             record_error(err, err_bit);
             return false;
         }
