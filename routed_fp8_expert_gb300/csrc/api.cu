@@ -233,9 +233,9 @@ int make_map_gateup(CUtensorMap *m, const void *ptr, uint64_t G, uint64_t H, uin
     return MOE_OK;
 }
 
-// Activation maps with box heights 16, 32, 64 and 128 rows.
+// Activation maps with box heights 16, 32, 64, 96 and 128 rows.
 int make_act_maps(ActMaps *m, const void *ptr, int elem_bytes, uint64_t rows, uint64_t cols) {
-    const uint32_t heights[kActBoxes] = {16, 32, 64, 128};
+    const uint32_t heights[kActBoxes] = {16, 32, 64, 96, 128};
     for (int i = 0; i < kActBoxes; ++i) MOE_CHECK(make_map(&m->box[i], ptr, elem_bytes, rows, cols, heights[i]));
     return MOE_OK;
 }
@@ -260,7 +260,7 @@ int make_map_kpair(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols
 }
 
 int make_act_maps_kpair(ActMaps *m, const void *ptr, uint64_t rows, uint64_t cols) {
-    const uint32_t heights[kActBoxes] = {16, 32, 64, 128};
+    const uint32_t heights[kActBoxes] = {16, 32, 64, 96, 128};
     for (int i = 0; i < kActBoxes; ++i) MOE_CHECK(make_map_kpair(&m->box[i], ptr, rows, cols, heights[i]));
     return MOE_OK;
 }

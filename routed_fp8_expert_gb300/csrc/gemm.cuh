@@ -60,7 +60,7 @@ constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
 constexpr int kATileBytes = kBM * kKBytes;  // 16 KB
 constexpr int kActBoxRows = 16;             // smallest activation TMA box height
-__device__ constexpr int kActBoxHeights[kActBoxes] = {16, 32, 64, 128};
+__device__ constexpr int kActBoxHeights[kActBoxes] = {16, 32, 64, 96, 128};
 constexpr int kMaxGroups = 1032;            // routed + shared experts, padded
 constexpr int kItemQ = 4;                   // depth of the producer -> consumers item queue
 
@@ -194,12 +194,11 @@ __device__ __forceinline__ void kb_range(const GemmArgs &a, const Item &I, int &
 }
 
 // Index into kActBoxHeights of the activation box of a tile of n rows: the
-// smallest that covers them, or the 128-row box (the MMA M dimension) for the
-// token-major kinds.
-template <bool kTokenMajor>
+// smallest that covers them. A token-major MMA still reads 128 rows (its M
+// dimension); the rows past the box hold an earlier stage's activations, and
+// their output rows (tokens past the tile's end) are never stored.
 __device__ __forceinline__ int act_box_index(int n) {
-    if (kTokenMajor) return 3;
-    return (n <= 16) ? 0 : (n <= 32) ? 1 : (n <= 64) ? 2 : 3;
+    return (n <= 16) ? 0 : (n <= 32) ? 1 : (n <= 64) ? 2 : (n <= 96) ? 3 : 4;
 }
 
 // Two floats as round-to-nearest bf16, the first in the low half (lower address).
@@ -386,7 +385,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             int kb0, kb1;
             kb_range(args, I, kb0, kb1);
             // one activation box per stage
-            const int box_i = act_box_index<C::kTM>(I.n);
+            const int box_i = act_box_index(I.n);
             // full boxes count toward the transaction bytes, including rows and a
             // K block beyond the tensor, which the TMA unit fills with zeros
             const uint32_t bytes = C::kKPS * (C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes);
@@ -467,7 +466,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 const int n_mma = C::kTM ? C::kPartCols : ((I.n + 15) & ~15);
                 const uint32_t idesc = idesc_make(kFmt, kFmt, kBM, n_mma);
                 // bytes of one K block's activation sub-tile inside a K-pair box
-                const uint32_t b_kb_bytes = kActBoxHeights[act_box_index<C::kTM>(I.n)] * kKBytes;
+                const uint32_t b_kb_bytes = kActBoxHeights[act_box_index(I.n)] * kKBytes;
                 for (int kb = kb0; kb < kb1; kb += C::kKPS) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) { ok = false; break; }
                     const uint32_t sbase = smem_u32(stages + stage * kStageBytes);

@@ -9,11 +9,10 @@ namespace moe {
 struct GemmArgs;
 enum class Kind;
 
-// Tensor maps of one activation matrix with box heights 16, 32, 64 and 128 rows
-// (128-byte swizzle; one K block, or a pair of K blocks for the token-major
-// kinds): a decode-sized token tile is loaded with the smallest single box that
-// covers its rows, a token-major tile with the 128-row box.
-constexpr int kActBoxes = 4;
+// Tensor maps of one activation matrix with box heights 16, 32, 64, 96 and 128
+// rows (128-byte swizzle; one K block, or a pair of K blocks for the K-pair
+// kind): a token tile is loaded with the smallest single box that covers its rows.
+constexpr int kActBoxes = 5;
 struct ActMaps {
     CUtensorMap box[kActBoxes];
 };
