@@ -99,9 +99,8 @@ template <Kind K, int BN> struct KindCfg {
     static constexpr int kHalfCols = kWide ? 64 : (kTM ? kBM : BN) / kGroups;  // accumulators per thread
     static constexpr int kChunks = kHalfCols / 16;
     static constexpr int kEpiWarps = 4 * kGroups;                 // one warp per TMEM lane quarter and group
-    // the K blocks' scales are copied by a warp of their own, or, in the 19-warp
-    // wide kinds, by the producer warp (18 warps leave 112 registers a thread)
-    static constexpr bool kScaleWarpOwn = kPromote && !kWide;
+    // the K blocks' scales are copied by a warp of their own, beside the producer
+    static constexpr bool kScaleWarpOwn = kPromote;
     static constexpr int kScaleWarp = 2 + kEpiWarps;
     static constexpr int kThreads = 64 + 32 * kEpiWarps + (kScaleWarpOwn ? 32 : 0);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
@@ -359,8 +358,6 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         int q = 0;
         uint32_t qphase = 0;
         int next_static = blockIdx.x;
-        int sslot = 0;                 // wide kinds: the producer also copies the scales
-        uint32_t sphase = 0;
         while (true) {
             int it = 0, got = 1;
             if (lane == 0) {
@@ -397,8 +394,6 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 constexpr int kRowsPerBlock = (KIND == Kind::DownPair || KIND == Kind::DownWide) ? 2 * kBM : kBM;
                 arow0 = I.g * args.a_rows_per_group + I.mb * kRowsPerBlock;
             }
-            const float *ws0 = nullptr, *ws1 = nullptr;
-            if constexpr (C::kWide) weight_scale_rows(I, ws0, ws1);
             bool ok = true;
             for (int kb = kb0; kb < kb1; kb += C::kKPS) {
                 int w = 1;
@@ -429,17 +424,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-                if constexpr (C::kWide) {
-                    if (lane == 0) w = mbar_wait(smem_u32(&sempty[sslot]), sphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
-                    w = __shfl_sync(0xffffffffu, w, 0);
-                    if (!w) { ok = false; break; }
-                    copy_scales(I, kb, sslot, ws0, ws1);
-                    if (++sslot == C::kScaleSlots) { sslot = 0; sphase ^= 1; }
-                }
             }
             if (!ok) break;
         }
-        if constexpr (C::kWide) cp_async_wait_all();   // the scale copies must land before the CTA may exit
         // every issued copy must land before the CTA may exit
         if (lane == 0)
             for (int s = 0; s < C::kStages; ++s)
@@ -890,9 +877,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     grouped_gemm_body<KIND, BN>(map_a, map_b, args);
 }
 
-// The 18-warp CTAs of the 256-row token-major kinds: 112 registers per thread
-// (18 x 32 x 112 = 64,512 of the SM's 65,536) for the epilogue's 64 accumulators
-// and 16 partials; the launch-bounds heuristic alone would allow 96.
+// The 19-warp CTAs of the 256-row token-major kinds: each sub-partition's register
+// file (16,384 registers) holds five of the warps at 96 registers a thread, enough
+// for the epilogue's 64 accumulators and a 16-column TMEM chunk.
 template <Kind KIND, int BN>
 __global__ void __maxnreg__(96)
 grouped_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ ActMaps map_b,
