@@ -221,10 +221,16 @@ template <Kind KIND, int BN> struct SmemLayout {
     static constexpr int kScaleStride = BN + 4;                                // floats per stage: BN act + 2 weight
     static constexpr size_t kScale = kRs + kMaxGroups * 4;                     // [kScaleSlots][kScaleStride]
     static constexpr size_t kCs = kScale + C::kScaleSlots * kScaleStride * 4;  // [warps][2][kATiles][HC], swap-AB
-    static constexpr size_t kAmax = kCs + (C::kTM ? 0 : C::kEpiWarps * 2 * C::kATiles * C::kHalfCols * 4);  // [groups][2][4][HC]
-    static constexpr size_t kEnd = kAmax + C::kGroups * 2 * 4 * C::kHalfCols * 4;
+    static constexpr size_t kAmax = kCs + (C::kTM ? 0 : C::kEpiWarps * 2 * C::kATiles * C::kHalfCols * 4);
+    // the h amax exchange: GateUp [groups][2][4][HC]; GateUpWide [2][4 groups][128 rows]
+    static constexpr size_t kAmaxBytes = (KIND == Kind::GateUp)       ? C::kGroups * 2 * 4 * C::kHalfCols * 4
+                                         : (KIND == Kind::GateUpWide) ? 2 * 4 * kBM * 4
+                                                                      : 0;
+    // DownWide: one 1 KB slot per epilogue warp to turn its rows into whole-line stores
+    static constexpr size_t kXpose = kAmax + kAmaxBytes;
+    static constexpr size_t kEnd = kXpose + ((KIND == Kind::DownWide) ? C::kEpiWarps * 1024 : 0);
     static constexpr size_t kLaunchBytes = kEnd + 1024;  // + alignment slack of the dynamic base
-    static_assert(kBars % 1024 == 0 && kScale % 16 == 0 && kCs % 16 == 0, "alignment");
+    static_assert(kBars % 1024 == 0 && kScale % 16 == 0 && kCs % 16 == 0 && kXpose % 16 == 0, "alignment");
     static_assert(kLaunchBytes <= 232448, "shared memory budget");
 };
 
@@ -264,6 +270,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     float *s_scale = reinterpret_cast<float *>(smem + L::kScale);  // scale slots
     float *s_cs = reinterpret_cast<float *>(smem + L::kCs);        // per-warp combined scales
     float *s_amax = reinterpret_cast<float *>(smem + L::kAmax);
+    uint8_t *s_xpose = smem + L::kXpose;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -641,17 +648,41 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                         h4[1] = make_uint4(w[4], w[5], w[6], w[7]);
                         if (grp == 0) args.hs_t[static_cast<size_t>(I.mb) * args.total_rows + row] = sq;
                     }
-                } else if (r < I.n) {
+                } else {
+                    // each lane holds its token's 64 outputs (128 bytes of bf16). Stored
+                    // directly, one 16-byte store instruction would touch 32 rows; instead
+                    // eight rows at a time pass through this warp's 1 KB slot (16-byte
+                    // chunk v of slot row q at chunk v ^ q: conflict-free both ways) and
+                    // leave as stores of whole 128-byte row segments, four rows each.
                     const int nout = args.num_mb * 2 * kBM;   // output features per row
-                    uint4 *o4 = reinterpret_cast<uint4 *>(args.out + row * nout + I.mb * 2 * kBM + grp * 64);
+                    uint4 w[HC / 8];
 #pragma unroll
                     for (int v = 0; v < HC / 8; ++v) {
-                        uint4 w;
-                        w.x = bf16x2_bits(acc[8 * v + 0], acc[8 * v + 1]);
-                        w.y = bf16x2_bits(acc[8 * v + 2], acc[8 * v + 3]);
-                        w.z = bf16x2_bits(acc[8 * v + 4], acc[8 * v + 5]);
-                        w.w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
-                        o4[v] = w;
+                        w[v].x = bf16x2_bits(acc[8 * v + 0], acc[8 * v + 1]);
+                        w[v].y = bf16x2_bits(acc[8 * v + 2], acc[8 * v + 3]);
+                        w[v].z = bf16x2_bits(acc[8 * v + 4], acc[8 * v + 5]);
+                        w[v].w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
+                    }
+                    uint8_t *slot = s_xpose + ew * 1024;
+                    __nv_bfloat16 *obase = args.out + static_cast<size_t>(I.mb) * 2 * kBM + grp * 64;
+#pragma unroll
+                    for (int pass = 0; pass < 4; ++pass) {
+                        if ((lane >> 3) == pass) {
+                            const int q = lane & 7;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                *reinterpret_cast<uint4 *>(slot + q * 128 + ((v ^ q) << 4)) = w[v];
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const int q = (lane >> 3) + 4 * half, c = lane & 7;
+                            const uint4 v4 = *reinterpret_cast<const uint4 *>(slot + q * 128 + ((c ^ q) << 4));
+                            const int tr = quad * 32 + pass * 8 + q;   // token row in the tile
+                            if (tr < I.n)
+                                *reinterpret_cast<uint4 *>(obase + static_cast<size_t>(I.row0 + tr) * nout + c * 8) = v4;
+                        }
+                        __syncwarp();
                     }
                 }
             } else if constexpr (C::kTM) {
