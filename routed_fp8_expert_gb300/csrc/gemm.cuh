@@ -560,6 +560,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 //   GateUpWide: gate [0, 32) and up [32, 64) of features 32*grp .. 32*grp+31
                 //   DownWide:   the 64 output rows 64*grp .. of the item's 256
                 const int r = quad * 32 + lane;
+                const bool quad_live = quad * 32 < I.n;   // warp-uniform
                 float acc[HC];
 #pragma unroll
                 for (int j = 0; j < HC; ++j) acc[j] = 0.f;
@@ -595,14 +596,17 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     const uint32_t tpart = t_lane + pb * C::kPartCols;
                     float p[16];
                     // one 16-column chunk in flight at a time (the 64 accumulators and
-                    // 16 partials fill the registers of the 19-warp CTA)
+                    // 16 partials fill the registers of the 19-warp CTA); a lane quarter
+                    // wholly past the tile's last token has nothing to fold
+                    if (quad_live) {
 #pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c) {
-                        tmem_ld16(tpart + chunk_col(c), p);
-                        tmem_wait_ld();
-                        const float s_c = (c < 2) ? s_lo : s_hi;
+                        for (int c = 0; c < C::kChunks; ++c) {
+                            tmem_ld16(tpart + chunk_col(c), p);
+                            tmem_wait_ld();
+                            const float s_c = (c < 2) ? s_lo : s_hi;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s_c, p[i], acc[c * 16 + i]);
+                            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s_c, p[i], acc[c * 16 + i]);
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -622,10 +626,12 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     const uint32_t ab = smem_u32(&amax_bar[quad * 2 + buf]);
                     float *xch = s_amax + buf * 4 * kBM;   // [group][token row]
                     float am = 0.f;
+                    if (quad_live) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        acc[j] = silu_f(acc[j]) * acc[32 + j];
-                        am = fmaxf(am, fabsf(acc[j]));
+                        for (int j = 0; j < 32; ++j) {
+                            acc[j] = silu_f(acc[j]) * acc[32 + j];
+                            am = fmaxf(am, fabsf(acc[j]));
+                        }
                     }
                     xch[grp * kBM + r] = am;
                     __syncwarp();
@@ -664,6 +670,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                         w[v].w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
                     }
                     uint8_t *slot = s_xpose + ew * 1024;
+                    if (quad_live) {
                     __nv_bfloat16 *obase = args.out + static_cast<size_t>(I.mb) * 2 * kBM + grp * 64;
 #pragma unroll
                     for (int pass = 0; pass < 4; ++pass) {
@@ -683,6 +690,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                                 *reinterpret_cast<uint4 *>(obase + static_cast<size_t>(I.row0 + tr) * nout + c * 8) = v4;
                         }
                         __syncwarp();
+                    }
                     }
                 }
             } else if constexpr (C::kTM) {

@@ -96,3 +96,11 @@ def test_kimi_decode_layer_sampled(kimi_weights):
 
 def test_kimi_prefill_layer_sampled(kimi_weights):
     _kimi(S.PREFILL, kimi_weights, n_tokens=3, seed=1)
+
+
+def test_kimi_skewed_layer_sampled(kimi_weights):
+    # the skewed batch (T=16384, +0.5 bias on 16 hot experts): the hot experts hold
+    # thousands of rows each, so dozens of 128-token tiles share every weight block
+    # and the dynamic scheduler hands them out
+    y = _kimi(S.SKEWED, kimi_weights, n_tokens=3, seed=2)
+    assert torch.isfinite(y.float()).all()
