@@ -104,16 +104,27 @@ int down_bn(const moe_cfg_t &c, int T) { return down_pair(c, T) ? 32 : 128; }
 
 int router_bn(int T) { return T <= 512 ? 32 : 128; }
 
-// Deterministic split-K of the router GEMM so that small batches still cover
-// the GPU in one wave: at most 148 work items, at least 4 K blocks (of 64
-// elements) per split.
+// Deterministic split-K of the router GEMM: the split count (1..8, at least 4 K
+// blocks of 64 elements per split, at most two waves of items) that minimises
+// waves x K blocks per split, the smaller count on ties. A 256-token batch thus
+// runs 6 splits in one wave; a 4096-token batch 3 splits in two waves instead of
+// 96 items in one.
 int router_splits(const moe_cfg_t &c, int T) {
     const int bn = router_bn(T);
     const int items = std::max(1, ((T + bn - 1) / bn) * ((c.E + 127) / 128));
-    int s = 148 / items;
-    const int max_by_k = std::max(1, (c.d / 64) / 4);
-    s = std::min(s, std::min(8, max_by_k));
-    return std::max(1, s);
+    const int num_kb = c.d / 64;
+    const int max_s = std::max(1, std::min(8, num_kb / 4));
+    const int sms = 148;   // work items per wave (the GPU's SMs less a small margin)
+    int best = 1;
+    long best_cost = -1;
+    // splits only while the split items fit two waves: beyond that each split adds a
+    // plane of partial logits for the top-k kernel to read and nothing to balance
+    for (int s = 1; s <= max_s && (s == 1 || items * s <= 2 * sms); ++s) {
+        const long waves = (static_cast<long>(items) * s + sms - 1) / sms;
+        const long cost = waves * ((num_kb + s - 1) / s);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
+    }
+    return best;
 }
 
 // ---------------------------------------------------------------- workspace
