@@ -329,11 +329,13 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * c.H;
     if (decode_regime(c, T)) {
-        // fused gate/up + SiLU*mul + h quantisation; static item order (uniform
-        // items, one token tile per routed expert)
+        // fused gate/up + SiLU*mul + h quantisation; items handed out by the global
+        // counter (one atomic per 56-K-block item), so the CTAs that finish early
+        // share the last partial round
         MOE_CHECK(make_map_gateup(&m13, w13, G, c.H, c.d));
         gu.hq = hq;
         gu.hs_t = hs;
+        gu.item_counter = ws.counters;
         MOE_CUDA(launch_grouped_gemm(Kind::GateUp, bn, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
         t_launches += 1;
         return MOE_OK;
@@ -372,7 +374,7 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
     dn.single_rows = -1;
     dn.row_start = ws.row_start;
     dn.tile_prefix = ws.tile_prefix_dn;
-    dn.item_counter = decode_regime(c, T) ? nullptr : ws.counters + 1;
+    dn.item_counter = ws.counters + 1;   // items handed out by the global counter
     dn.act_scale_t = hs;
     dn.w_scale = w2_s;
     dn.a_rows_per_group = c.d;
