@@ -71,3 +71,11 @@ def test_decode_down_with_odd_block_count():
 def test_wide_k_and_many_blocks():
     shape = S.MoEShape("wide", T=48, d=2048, E=16, topk=4, H=640, n_shared=1)
     _run(shape, seed=2)
+
+
+def test_wide_tiles_with_odd_block_counts():
+    # 100 rows per routed expert (128-token tiles) with d = H = 384: the gate/up items
+    # run three K blocks, and the down projection (three 128-row output blocks) takes
+    # the one-block token-major kernel, whose last K pair holds a single K block
+    shape = S.MoEShape("odd_wide", T=400, d=384, E=32, topk=8, H=384)
+    assert _run(shape, seed=5) == 9 * 400
