@@ -31,6 +31,10 @@ What it computes, and where each step comes from:
   dynamically in 1x128 groups with fp32 scales ("Kimi-K2-Base", Pretraining
   recipe: Training precision), scale = amax / 448.
 * Combine: y = shared(x) + sum_j w_j * expert_{I_j}(x).
+* Around the FFN ("Kimi K2 · Dense transformer block", Sources; "Kimi-K2-Base",
+  Normalization and stability): the post-attention RMSNorm (eps 1e-6) that
+  produces the layer input, and the residual addition after it, followed by the
+  next block's input RMSNorm.
 
 Parity pins for every function live in ``tests/test_oracle_*.py``. The layer
 output as a whole has no worked example on the pages: its end-to-end value is
@@ -314,6 +318,69 @@ def dense_swiglu(x, w13, w13_s, w2, w2_s, tokens=None):
     xq, xs = quantize_1x128(x[toks])
     o, _, _ = swiglu_fp8(xq, xs, w13[0], w13s[0], w13[1], w13s[1], w2, w2s)
     return o, toks
+
+
+# ---------------------------------------------------------------------------
+# The block around the FFN: RMSNorm and the residual addition
+# ---------------------------------------------------------------------------
+
+RMS_NORM_EPS = 1e-6   # "Kimi-K2-Base", Normalization and stability: Norm epsilon
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bfloat16 value (8 significant bits), ties
+    to the even significand, in one step from the exact value. Returned as fp64."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)                       # v = m * 2**e with 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)   # np.rint: half to even
+
+
+def rms_norm(h, gamma, eps: float = RMS_NORM_EPS) -> np.ndarray:
+    """RMSNorm of each row of h [T, d] with the per-feature weight gamma [d]:
+    y = gamma * h / sqrt(mean(h^2) + eps), in fp64 over the bf16 values of h and
+    gamma, rounded once to bf16 ("Kimi-K2-Base", Normalization and stability:
+    Norm RMSNorm, placement pre, epsilon 1e-06; "Kimi K2 · Dense transformer
+    block", Parameters: one 7,168-weight RMSNorm before the attention and one
+    before the MLP). Returns fp64 values that are bf16 numbers."""
+    h = _np(h).astype(np.float64)
+    g = _np(gamma).astype(np.float64)
+    inv = 1.0 / np.sqrt((h * h).mean(axis=1, keepdims=True) + eps)
+    return round_bf16(h * inv * g)
+
+
+def residual_add(residual, y) -> np.ndarray:
+    """The block's second residual addition, h_next = residual + mlp(x), on bf16
+    tensors: the FFN output is a bf16 tensor (y rounded to bf16 first) and the
+    sum of the two bf16 values is rounded to bf16 ("Kimi K2 · Dense transformer
+    block", Sources: the block's forward adds the residual after the MLP)."""
+    r = _np(residual).astype(np.float64)
+    return round_bf16(r + round_bf16(_np(y).astype(np.float64)))
+
+
+def moe_block_ffn(h, gamma_post, w_gate, bias, experts, topk: int, route_scale: float,
+                  gamma_next=None, eps: float = RMS_NORM_EPS, n_shared: int = 1,
+                  tokens=None, idx_override=None):
+    """The FFN half of a MoE block: x = RMSNorm_post(h), y = moe_layer(x),
+    h_next = h + y, and, when gamma_next is given, the next block's normalised
+    input RMSNorm_next(h_next) ("Kimi K2 · Dense transformer block", Sources:
+    residual = h; h = post_attention_layernorm(h); h = mlp(h); h = residual + h;
+    the next block starts with its input_layernorm).
+    Returns the moe_layer() dict plus x (bf16 values, all tokens), h_next and
+    x_next (rows of ``tokens``; other rows NaN)."""
+    h = _np(h).astype(np.float32)
+    x = rms_norm(h, gamma_post, eps).astype(np.float32)
+    out = moe_layer(x, w_gate, bias, experts, topk, route_scale, n_shared=n_shared, tokens=tokens,
+                    idx_override=idx_override)
+    toks = out["tokens"]
+    h_next = np.full(h.shape, np.nan)
+    h_next[toks] = residual_add(h[toks], out["y"][toks])
+    out["x"] = x
+    out["h_next"] = h_next
+    if gamma_next is not None:
+        x_next = np.full(h.shape, np.nan)
+        x_next[toks] = rms_norm(h_next[toks], gamma_next, eps)
+        out["x_next"] = x_next
+    return out
 
 
 # ---------------------------------------------------------------------------
