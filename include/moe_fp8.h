@@ -162,6 +162,30 @@ int moe_expert_down_fp8(const uint8_t *hq, const float *hs, const int32_t *offse
 int moe_combine(const void *o, const float *topk_w, const int32_t *inv_pos,
                 const moe_cfg_t *cfg, int T, void *y, void *stream);
 
+/* The block's pieces next to the layer ("Kimi K2 · Dense transformer block",
+ * Sources: residual = h; h = post_attention_layernorm(h); h = mlp(h);
+ * h = residual + h; "Kimi-K2-Base", Normalization and stability: RMSNorm, pre-norm,
+ * epsilon 1e-06). RMSNorm of a bf16 row: y = bf16(h * gamma / sqrt(mean(h^2) + eps)),
+ * the sum of squares in fp32 (fixed order), IEEE square root and division.
+ *
+ * moe_rmsnorm_quant_fp8: the layer input from the residual stream in one pass:
+ *   h [rows, cols] bf16; gamma [cols] bf16; y [rows, cols] bf16 (may be NULL: not
+ *   written); q, s the 1x128 quantisation of the bf16 y values, bit-identical to
+ *   moe_quant_fp8_1x128 applied to y (s layout as there). cols % 128 == 0.
+ *   Pointers 16-byte aligned; rows == 0 is a no-op. */
+int moe_rmsnorm_quant_fp8(const void *h, const void *gamma, float eps, int rows, int cols,
+                          void *y, uint8_t *q, float *s, int s_transposed, void *stream);
+
+/* moe_combine_residual_rmsnorm: moe_combine (same summation order) rounded to bf16
+ * as the FFN output y, then h_out = bf16(residual + y) (the block's second residual
+ * addition), and, when gamma is not NULL, x_next = the next block's input RMSNorm
+ * of h_out (gamma and x_next both given or both NULL).
+ * o, topk_w, inv_pos as in moe_combine; residual, h_out, x_next [T, d] bf16;
+ * gamma [d] bf16. */
+int moe_combine_residual_rmsnorm(const void *o, const float *topk_w, const int32_t *inv_pos,
+                                 const moe_cfg_t *cfg, int T, const void *residual, const void *gamma,
+                                 float eps, void *h_out, void *x_next, void *stream);
+
 /* The whole layer: route, quantise x, permute, grouped expert GEMMs, combine.
  * x [T, d] bf16; w_gate [E, d] bf16; bias [E] fp32; weights as in
  * moe_expert_gemm_fp8; y [T, d] bf16. topk_idx / topk_w [T, topk] receive the

@@ -97,6 +97,20 @@ def gen_x(T: int, d: int, seed: int = 0, device="cpu", name: str = "x") -> torch
     return randn((T, d), 1.0, device, seed, name, dtype=torch.bfloat16)
 
 
+def gen_residual(T: int, d: int, seed: int = 0, device="cpu", std: float = 1.0, name: str = "residual") -> torch.Tensor:
+    """Residual-stream rows h ~ N(0, std^2) times a per-row factor 10^U(-1, 1)
+    (rows of different magnitude, as RMSNorm sees them), bf16 [T, d]."""
+    g = _gen(device, seed, name)
+    f = 10.0 ** (torch.rand((T, 1), generator=g, device=device) * 2.0 - 1.0)
+    return (torch.randn((T, d), generator=g, device=device) * std * f).to(torch.bfloat16)
+
+
+def gen_norm_weight(d: int, seed: int = 0, device="cpu", name: str = "norm") -> torch.Tensor:
+    """RMSNorm weight gamma ~ U(0.5, 1.5), bf16 [d]."""
+    g = _gen(device, seed, name)
+    return (torch.rand(d, generator=g, device=device) + 0.5).to(torch.bfloat16)
+
+
 def gen_router(shape: MoEShape, seed: int = 0, device="cpu"):
     """Router weight W_g ~ N(0, 0.02) bf16 [E, d] and selection bias ~ N(0, 0.01) fp32 [E].
 

@@ -42,6 +42,9 @@ _SIGS = {
     "moe_expert_down_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _c_size,
                                      _vp]),
     "moe_combine": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp]),
+    "moe_rmsnorm_quant_fp8": (_c_int, [_vp, _vp, ctypes.c_float, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp]),
+    "moe_combine_residual_rmsnorm": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp,
+                                              ctypes.c_float, _vp, _vp, _vp]),
     "moe_layer_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp,
                                    _vp, _vp, _c_size, _vp]),
     "dense_swiglu_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
@@ -213,6 +216,36 @@ def combine(o, topk_w, inv_pos, cfg: MoeCfg, T: int):
     y = torch.empty((T, cfg.d), dtype=torch.bfloat16, device=o.device)
     _check(load().moe_combine(_p(o), _p(topk_w), _p(inv_pos), ctypes.byref(cfg), T, _p(y), _stream(o.device)))
     return y
+
+
+RMS_NORM_EPS = 1e-6
+
+
+def rmsnorm_quant_fp8(h, gamma, eps: float = RMS_NORM_EPS, write_y: bool = True, s_transposed: bool = False):
+    """moe_rmsnorm_quant_fp8: h [rows, cols] bf16, gamma [cols] bf16 ->
+    (y bf16 [rows, cols] or None, q uint8 [rows, cols], s fp32)."""
+    _cuda(h, gamma)
+    rows, cols = h.shape
+    dev = h.device
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) if write_y else None
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    s = torch.empty(((cols // 128, rows) if s_transposed else (rows, cols // 128)), dtype=torch.float32, device=dev)
+    _check(load().moe_rmsnorm_quant_fp8(_p(h), _p(gamma), float(eps), rows, cols, _p(y) if y is not None else None,
+                                        _p(q), _p(s), int(s_transposed), _stream(dev)))
+    return y, q, s
+
+
+def combine_residual_rmsnorm(o, topk_w, inv_pos, cfg: MoeCfg, T: int, residual, gamma=None,
+                             eps: float = RMS_NORM_EPS):
+    """moe_combine_residual_rmsnorm -> (h_out bf16 [T, d], x_next bf16 [T, d] or None)."""
+    _cuda(o, topk_w, inv_pos, residual)
+    dev = o.device
+    h_out = torch.empty((T, cfg.d), dtype=torch.bfloat16, device=dev)
+    x_next = torch.empty((T, cfg.d), dtype=torch.bfloat16, device=dev) if gamma is not None else None
+    _check(load().moe_combine_residual_rmsnorm(_p(o), _p(topk_w), _p(inv_pos), ctypes.byref(cfg), T, _p(residual),
+                                               _p(gamma) if gamma is not None else None, float(eps), _p(h_out),
+                                               _p(x_next) if x_next is not None else None, _stream(dev)))
+    return h_out, x_next
 
 
 def layer_forward(x, w_gate, bias, experts, cfg: MoeCfg, ws=None, y=None, want_routing=False):

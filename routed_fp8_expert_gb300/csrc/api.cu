@@ -565,6 +565,52 @@ int moe_combine(const void *o, const float *topk_w, const int32_t *inv_pos, cons
     return MOE_OK;
 }
 
+int moe_rmsnorm_quant_fp8(const void *h, const void *gamma, float eps, int rows, int cols, void *y, uint8_t *q,
+                          float *s, int s_transposed, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_T(rows));
+    if (cols <= 0 || cols % 128 || cols > 65536)
+        return fail(MOE_ERR_UNSUPPORTED, "cols=%d must be a positive multiple of 128 (at most 65536)", cols);
+    if (!(eps >= 0.f)) return fail(MOE_ERR_ARG, "eps must be a non-negative number");
+    if (rows == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(h, "h"));
+    MOE_CHECK(check_ptr(gamma, "gamma"));
+    if (y) MOE_CHECK(check_ptr(y, "y"));
+    MOE_CHECK(check_ptr(q, "q"));
+    if (!s) return fail(MOE_ERR_ARG, "s is NULL");
+    MOE_CUDA(launch_rmsnorm_quant(h, gamma, eps, rows, cols, y, q, s, s_transposed != 0,
+                                  static_cast<cudaStream_t>(stream)),
+             "RMSNorm quantise launch");
+    t_launches = 1;
+    return MOE_OK;
+}
+
+int moe_combine_residual_rmsnorm(const void *o, const float *topk_w, const int32_t *inv_pos, const moe_cfg_t *cfg,
+                                 int T, const void *residual, const void *gamma, float eps, void *h_out,
+                                 void *x_next, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (!(eps >= 0.f)) return fail(MOE_ERR_ARG, "eps must be a non-negative number");
+    if ((gamma == nullptr) != (x_next == nullptr))
+        return fail(MOE_ERR_ARG, "gamma and x_next are both given or both NULL");
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(o, "o"));
+    MOE_CHECK(check_ptr(topk_w, "topk_w"));
+    MOE_CHECK(check_ptr(inv_pos, "inv_pos"));
+    MOE_CHECK(check_ptr(residual, "residual"));
+    MOE_CHECK(check_ptr(h_out, "h_out"));
+    if (gamma) {
+        MOE_CHECK(check_ptr(gamma, "gamma"));
+        MOE_CHECK(check_ptr(x_next, "x_next"));
+    }
+    MOE_CUDA(launch_combine_residual_rmsnorm(o, topk_w, inv_pos, T, cfg->topk, cfg->n_shared, cfg->d, residual,
+                                             gamma, eps, h_out, x_next, static_cast<cudaStream_t>(stream)),
+             "combine + residual + RMSNorm launch");
+    t_launches = 1;
+    return MOE_OK;
+}
+
 int moe_layer_forward(const void *x, const void *w_gate, const float *bias, const uint8_t *w13, const float *w13_s,
                       const uint8_t *w2, const float *w2_s, const moe_cfg_t *cfg, int T, void *y, int32_t *topk_idx,
                       float *topk_w, void *workspace, size_t workspace_bytes, void *stream) {

@@ -65,4 +65,22 @@ cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos
     return cudaGetLastError();
 }
 
+cudaError_t launch_rmsnorm_quant(const void *h, const void *gamma, float eps, int rows, int cols, void *y,
+                                 uint8_t *q, float *s, bool s_transposed, cudaStream_t stream) {
+    rmsnorm_quant_kernel<<<rows, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(h),
+                                                    static_cast<const __nv_bfloat16 *>(gamma), eps, cols,
+                                                    static_cast<__nv_bfloat16 *>(y), q, s, rows, s_transposed ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_residual_rmsnorm(const void *o, const float *w, const int32_t *inv_pos, int T, int k,
+                                            int S, int d, const void *residual, const void *gamma, float eps,
+                                            void *h_out, void *x_next, cudaStream_t stream) {
+    combine_residual_rmsnorm_kernel<<<T, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d, static_cast<const __nv_bfloat16 *>(residual),
+        static_cast<const __nv_bfloat16 *>(gamma), eps, static_cast<__nv_bfloat16 *>(h_out),
+        static_cast<__nv_bfloat16 *>(x_next));
+    return cudaGetLastError();
+}
+
 }  // namespace moe

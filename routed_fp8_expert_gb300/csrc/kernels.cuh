@@ -1,5 +1,7 @@
 // Bandwidth- and latency-bound kernels of the MoE layer: 1x128 activation
-// quantisation, router top-k, token permutation and the weighted combine.
+// quantisation, router top-k, token permutation and the weighted combine, and
+// the block pieces around the layer (RMSNorm + quantisation of its input; the
+// combine fused with the residual addition and the next block's RMSNorm).
 #pragma once
 #include "ptx.cuh"
 
@@ -378,6 +380,167 @@ __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float 
 #pragma unroll
     for (int i = 0; i < 4; ++i) oh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
     reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * d)[v] = out;
+}
+
+// ------------------------------------------------------------------ block pieces
+// Sum of one float per thread over the CTA (blockDim a multiple of 32), in a fixed
+// order: lanes by xor butterfly, then the warps' sums by warp 0. Every thread gets
+// the total.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float t = (lane < static_cast<int>(blockDim.x >> 5)) ? red[lane] : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(kFull, t, off);
+        if (lane == 0) red[32] = t;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+// 1 / sqrt(mean of squares + eps), with IEEE square root and division.
+__device__ __forceinline__ float rms_inverse(float sum_sq, int n, float eps) {
+    return 1.0f / sqrtf(sum_sq / static_cast<float>(n) + eps);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&v)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __low2float(h[i]);
+        v[2 * i + 1] = __high2float(h[i]);
+    }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
+    uint4 out;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    return out;
+}
+
+// RMSNorm of one bf16 row per CTA, y = bf16(h * inv * gamma) with
+// inv = 1 / sqrt(mean(h^2) + eps), followed by the 1x128 quantisation of the bf16
+// y values with the arithmetic of quant_1x128_kernel. Pass 1 sums h^2 in fp32 over
+// 8-element units (fixed order); pass 2 re-reads the row: each 128-wide group is
+// 16 consecutive units, held by a half-warp (blockDim a multiple of 32, cols a
+// multiple of 128, so a half-warp is wholly inside or outside the row).
+__global__ void rmsnorm_quant_kernel(const __nv_bfloat16 *__restrict__ h, const __nv_bfloat16 *__restrict__ gamma,
+                                     float eps, int cols, __nv_bfloat16 *__restrict__ y, uint8_t *__restrict__ q,
+                                     float *__restrict__ s, int rows, int s_transposed) {
+    __shared__ float red[33];
+    const int r = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int nunits = cols / 8;
+    const uint4 *hr = reinterpret_cast<const uint4 *>(h + static_cast<size_t>(r) * cols);
+    const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
+    float ss = 0.f;
+    for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
+        float v[8];
+        unpack_bf16x8(hr[u], v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+    }
+    const float inv = rms_inverse(block_sum(ss, red), cols, eps);
+    const unsigned half_mask = 0xffffu << (lane & 16);
+    for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
+        float v[8], g[8];
+        unpack_bf16x8(hr[u], v);
+        unpack_bf16x8(gr[u], g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = v[i] * inv * g[i];
+        const uint4 packed = pack_bf16x8(v);
+        if (y) reinterpret_cast<uint4 *>(y + static_cast<size_t>(r) * cols)[u] = packed;
+        unpack_bf16x8(packed, v);   // the bf16 values are what gets quantised
+        unsigned m = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = max(m, __float_as_uint(fabsf(v[i])));
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(half_mask, m, off, 16));
+        const float amax = __uint_as_float(m);
+        const float sc = amax / 448.0f;
+        uint2 codes = make_uint2(0u, 0u);
+        if (amax != 0.f) {
+            codes.x = static_cast<uint32_t>(e4m3x2(v[0] / sc, v[1] / sc)) | (static_cast<uint32_t>(e4m3x2(v[2] / sc, v[3] / sc)) << 16);
+            codes.y = static_cast<uint32_t>(e4m3x2(v[4] / sc, v[5] / sc)) | (static_cast<uint32_t>(e4m3x2(v[6] / sc, v[7] / sc)) << 16);
+        }
+        reinterpret_cast<uint2 *>(q + static_cast<size_t>(r) * cols)[u] = codes;
+        if ((lane & 15) == 0) {
+            const int g128 = u >> 4;
+            s[s_transposed ? (static_cast<size_t>(g128) * rows + r) : (static_cast<size_t>(r) * (cols / 128) + g128)] = sc;
+        }
+    }
+}
+
+// The combine of combine_kernel (same summation order, rounded to bf16 as the FFN
+// output), plus the block's residual addition h = bf16(residual + y), and, when
+// gamma is given, the next block's input RMSNorm x = bf16(h * inv * gamma) of that
+// bf16 row. One CTA per token; pass 2 re-reads the thread's own h writes.
+__global__ void combine_residual_rmsnorm_kernel(const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w,
+                                                const int32_t *__restrict__ inv_pos, int T, int k, int S, int d,
+                                                const __nv_bfloat16 *__restrict__ residual,
+                                                const __nv_bfloat16 *__restrict__ gamma, float eps,
+                                                __nv_bfloat16 *__restrict__ h_out, __nv_bfloat16 *__restrict__ x_next) {
+    __shared__ int32_t s_pos[32];
+    __shared__ float s_w[32];
+    __shared__ float red[33];
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) {
+        s_pos[threadIdx.x] = inv_pos[static_cast<size_t>(t) * k + threadIdx.x];
+        s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
+    }
+    __syncthreads();
+    const int nunits = d / 8;
+    const uint4 *rr = reinterpret_cast<const uint4 *>(residual + static_cast<size_t>(t) * d);
+    uint4 *hr = reinterpret_cast<uint4 *>(h_out + static_cast<size_t>(t) * d);
+    float ss = 0.f;
+    for (int v = threadIdx.x; v < nunits; v += blockDim.x) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int sh = 0; sh < S; ++sh) {
+            float e[8];
+            unpack_bf16x8(reinterpret_cast<const uint4 *>(o + (static_cast<size_t>(k) * T + static_cast<size_t>(sh) * T + t) * d)[v], e);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += e[i];
+        }
+        for (int j = 0; j < k; ++j) {
+            if (s_pos[j] < 0) continue;
+            float e[8];
+            unpack_bf16x8(reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v], e);
+            const float wj = s_w[j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, e[i], acc[i]);
+        }
+        float yb[8], res[8];
+        unpack_bf16x8(pack_bf16x8(acc), yb);   // the FFN output is a bf16 tensor
+        unpack_bf16x8(rr[v], res);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) yb[i] = res[i] + yb[i];
+        const uint4 hp = pack_bf16x8(yb);
+        hr[v] = hp;
+        if (gamma) {
+            unpack_bf16x8(hp, yb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = fmaf(yb[i], yb[i], ss);
+        }
+    }
+    if (!gamma) return;   // uniform over the CTA
+    const float inv = rms_inverse(block_sum(ss, red), d, eps);
+    const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
+    for (int v = threadIdx.x; v < nunits; v += blockDim.x) {
+        float hv[8], g[8];
+        unpack_bf16x8(hr[v], hv);
+        unpack_bf16x8(gr[v], g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hv[i] = hv[i] * inv * g[i];
+        reinterpret_cast<uint4 *>(x_next + static_cast<size_t>(t) * d)[v] = pack_bf16x8(hv);
+    }
 }
 
 }  // namespace moe
