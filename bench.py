@@ -416,6 +416,7 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = tokens_total / (e2e_ms * 1e-3)
     same = torch.equal(yd, y)
+    pieces = time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -441,8 +442,51 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
                 "d2h_bytes_per_step": T * d * 2, "api": "moe_layer_forward", "matches_step_output": bool(same)},
         "gpu_launches": launches,
         "clocks": clk,
+        "block_pieces": pieces,
     }
     return line, (x, wg, b, ex, idx)
+
+
+def time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks, n=50):
+    """The block's kernels next to the layer, timed apart from the step with CUDA
+    events on the step's own tensors (x as the residual stream, o and the routing of
+    the last step): RMSNorm + quantise of the layer input, and the combine fused with
+    the residual addition and the next block's RMSNorm. HBM-bound: algorithmic bytes
+    (reads + writes) over the time, against the measured copy bandwidth."""
+    import ctypes
+    T, d, k, Sh = shape.T, shape.d, shape.topk, shape.n_shared
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    gamma = S.gen_norm_weight(d, seed=0, device=dev)
+    xb = torch.empty_like(x)
+    xq = torch.empty((T, d), dtype=torch.uint8, device=dev)
+    sx = torch.empty((T, d // 128), dtype=torch.float32, device=dev)
+    h_out = torch.empty_like(x)
+    x_next = torch.empty_like(x)
+    eps = ctypes.c_float(1e-6)
+    calls = {
+        "rmsnorm_quant_kernel": (lambda: L.moe_rmsnorm_quant_fp8(P(x), P(gamma), eps, T, d, P(xb), P(xq), P(sx), 0, st),
+                                 T * d * 2 + d * 2 + T * d * 2 + T * d + T * (d // 128) * 4),
+        "combine_residual_rmsnorm_kernel": (
+            lambda: L.moe_combine_residual_rmsnorm(P(o), P(w), P(inv_pos), ctypes.byref(cfg), T, P(x), P(gamma), eps,
+                                                   P(h_out), P(x_next), st),
+            (k + Sh) * T * d * 2 + T * k * 8 + T * d * 2 + d * 2 + 2 * T * d * 2),
+    }
+    out = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(3):
+            if fn() != 0:
+                raise RuntimeError(L.moe_last_error_string().decode())
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / n
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "alg_bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    return out
 
 
 def run_dense(args, shape, rank, world, dev, peaks):

@@ -65,9 +65,17 @@ cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos
     return cudaGetLastError();
 }
 
+// Threads of a one-row-per-CTA kernel: kRowUnits 8-element units each, a multiple
+// of 32, at most 1024 (longer rows loop). A d = 7168 row: 224 threads.
+static int row_threads(int cols) {
+    const int units = cols / 8;
+    const int t = ((units + kRowUnits - 1) / kRowUnits + 31) / 32 * 32;
+    return t < 1024 ? t : 1024;
+}
+
 cudaError_t launch_rmsnorm_quant(const void *h, const void *gamma, float eps, int rows, int cols, void *y,
                                  uint8_t *q, float *s, bool s_transposed, cudaStream_t stream) {
-    rmsnorm_quant_kernel<<<rows, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(h),
+    rmsnorm_quant_kernel<<<rows, row_threads(cols), 0, stream>>>(static_cast<const __nv_bfloat16 *>(h),
                                                     static_cast<const __nv_bfloat16 *>(gamma), eps, cols,
                                                     static_cast<__nv_bfloat16 *>(y), q, s, rows, s_transposed ? 1 : 0);
     return cudaGetLastError();
@@ -76,7 +84,7 @@ cudaError_t launch_rmsnorm_quant(const void *h, const void *gamma, float eps, in
 cudaError_t launch_combine_residual_rmsnorm(const void *o, const float *w, const int32_t *inv_pos, int T, int k,
                                             int S, int d, const void *residual, const void *gamma, float eps,
                                             void *h_out, void *x_next, cudaStream_t stream) {
-    combine_residual_rmsnorm_kernel<<<T, 256, 0, stream>>>(
+    combine_residual_rmsnorm_kernel<<<T, row_threads(d), 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d, static_cast<const __nv_bfloat16 *>(residual),
         static_cast<const __nv_bfloat16 *>(gamma), eps, static_cast<__nv_bfloat16 *>(h_out),
         static_cast<__nv_bfloat16 *>(x_next));

@@ -9,6 +9,15 @@ namespace moe {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&v)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __low2float(h[i]);
+        v[2 * i + 1] = __high2float(h[i]);
+    }
+}
+
 // ------------------------------------------------------------------ quantise
 // One warp per 128-wide group: lane l holds elements 4l..4l+3.
 // s = amax / 448 (IEEE fp32 division), q = e4m3(x / s) (IEEE division, RNE,
@@ -407,14 +416,6 @@ __device__ __forceinline__ float rms_inverse(float sum_sq, int n, float eps) {
     return 1.0f / sqrtf(sum_sq / static_cast<float>(n) + eps);
 }
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&v)[8]) {
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __low2float(h[i]);
-        v[2 * i + 1] = __high2float(h[i]);
-    }
-}
 
 __device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
     uint4 out;
@@ -424,33 +425,56 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
     return out;
 }
 
+// Units (8 bf16 each) of a row that a thread of the one-row-per-CTA kernels loads
+// up front and keeps in registers between their two passes; longer rows loop and
+// re-read.
+constexpr int kRowUnits = 4;
+
 // RMSNorm of one bf16 row per CTA, y = bf16(h * inv * gamma) with
 // inv = 1 / sqrt(mean(h^2) + eps), followed by the 1x128 quantisation of the bf16
-// y values with the arithmetic of quant_1x128_kernel. Pass 1 sums h^2 in fp32 over
-// 8-element units (fixed order); pass 2 re-reads the row: each 128-wide group is
-// 16 consecutive units, held by a half-warp (blockDim a multiple of 32, cols a
-// multiple of 128, so a half-warp is wholly inside or outside the row).
-__global__ void rmsnorm_quant_kernel(const __nv_bfloat16 *__restrict__ h, const __nv_bfloat16 *__restrict__ gamma,
-                                     float eps, int cols, __nv_bfloat16 *__restrict__ y, uint8_t *__restrict__ q,
-                                     float *__restrict__ s, int rows, int s_transposed) {
+// y values with the arithmetic of quant_1x128_kernel. Thread t holds units
+// t + i * blockDim (i < kRowUnits): pass 1 sums h^2 in fp32 in that fixed order;
+// pass 2 normalises, and each 128-wide group is 16 consecutive units held by a
+// half-warp (blockDim a multiple of 32, cols a multiple of 128, so a half-warp is
+// wholly inside or outside the row).
+__global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const __nv_bfloat16 *__restrict__ h,
+                                                             const __nv_bfloat16 *__restrict__ gamma, float eps,
+                                                             int cols, __nv_bfloat16 *__restrict__ y,
+                                                             uint8_t *__restrict__ q, float *__restrict__ s, int rows,
+                                                             int s_transposed) {
     __shared__ float red[33];
     const int r = blockIdx.x;
     const int lane = threadIdx.x & 31;
     const int nunits = cols / 8;
+    const int nthr = static_cast<int>(blockDim.x);
+    const bool cached = nunits <= kRowUnits * nthr;
     const uint4 *hr = reinterpret_cast<const uint4 *>(h + static_cast<size_t>(r) * cols);
     const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
+    uint4 row[kRowUnits];
     float ss = 0.f;
-    for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
+    auto accumulate = [&](const uint4 &raw) {
         float v[8];
-        unpack_bf16x8(hr[u], v);
+        unpack_bf16x8(raw, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+    };
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kRowUnits; ++i) {
+            const int u = threadIdx.x + i * nthr;
+            if (u < nunits) row[i] = hr[u];
+        }
+#pragma unroll
+        for (int i = 0; i < kRowUnits; ++i)
+            if (threadIdx.x + i * nthr < nunits) accumulate(row[i]);
+    } else {
+        for (int u = threadIdx.x; u < nunits; u += nthr) accumulate(hr[u]);
     }
     const float inv = rms_inverse(block_sum(ss, red), cols, eps);
     const unsigned half_mask = 0xffffu << (lane & 16);
-    for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
+    auto emit = [&](int u, const uint4 &raw) {
         float v[8], g[8];
-        unpack_bf16x8(hr[u], v);
+        unpack_bf16x8(raw, v);
         unpack_bf16x8(gr[u], g);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = v[i] * inv * g[i];
@@ -466,26 +490,37 @@ __global__ void rmsnorm_quant_kernel(const __nv_bfloat16 *__restrict__ h, const 
         const float sc = amax / 448.0f;
         uint2 codes = make_uint2(0u, 0u);
         if (amax != 0.f) {
-            codes.x = static_cast<uint32_t>(e4m3x2(v[0] / sc, v[1] / sc)) | (static_cast<uint32_t>(e4m3x2(v[2] / sc, v[3] / sc)) << 16);
-            codes.y = static_cast<uint32_t>(e4m3x2(v[4] / sc, v[5] / sc)) | (static_cast<uint32_t>(e4m3x2(v[6] / sc, v[7] / sc)) << 16);
+            float d8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d8[i] = v[i] / sc;
+            codes.x = static_cast<uint32_t>(e4m3x2(d8[0], d8[1])) | (static_cast<uint32_t>(e4m3x2(d8[2], d8[3])) << 16);
+            codes.y = static_cast<uint32_t>(e4m3x2(d8[4], d8[5])) | (static_cast<uint32_t>(e4m3x2(d8[6], d8[7])) << 16);
         }
         reinterpret_cast<uint2 *>(q + static_cast<size_t>(r) * cols)[u] = codes;
         if ((lane & 15) == 0) {
             const int g128 = u >> 4;
             s[s_transposed ? (static_cast<size_t>(g128) * rows + r) : (static_cast<size_t>(r) * (cols / 128) + g128)] = sc;
         }
+    };
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kRowUnits; ++i) {
+            const int u = threadIdx.x + i * nthr;
+            if (u < nunits) emit(u, row[i]);
+        }
+    } else {
+        for (int u = threadIdx.x; u < nunits; u += nthr) emit(u, hr[u]);
     }
 }
 
 // The combine of combine_kernel (same summation order, rounded to bf16 as the FFN
 // output), plus the block's residual addition h = bf16(residual + y), and, when
 // gamma is given, the next block's input RMSNorm x = bf16(h * inv * gamma) of that
-// bf16 row. One CTA per token; pass 2 re-reads the thread's own h writes.
-__global__ void combine_residual_rmsnorm_kernel(const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w,
-                                                const int32_t *__restrict__ inv_pos, int T, int k, int S, int d,
-                                                const __nv_bfloat16 *__restrict__ residual,
-                                                const __nv_bfloat16 *__restrict__ gamma, float eps,
-                                                __nv_bfloat16 *__restrict__ h_out, __nv_bfloat16 *__restrict__ x_next) {
+// bf16 row. One CTA per token; thread t holds units t + i * blockDim as above.
+__global__ void __launch_bounds__(1024) combine_residual_rmsnorm_kernel(
+    const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w, const int32_t *__restrict__ inv_pos, int T,
+    int k, int S, int d, const __nv_bfloat16 *__restrict__ residual, const __nv_bfloat16 *__restrict__ gamma,
+    float eps, __nv_bfloat16 *__restrict__ h_out, __nv_bfloat16 *__restrict__ x_next) {
     __shared__ int32_t s_pos[32];
     __shared__ float s_w[32];
     __shared__ float red[33];
@@ -496,10 +531,13 @@ __global__ void combine_residual_rmsnorm_kernel(const __nv_bfloat16 *__restrict_
     }
     __syncthreads();
     const int nunits = d / 8;
+    const int nthr = static_cast<int>(blockDim.x);
+    const bool cached = nunits <= kRowUnits * nthr;
     const uint4 *rr = reinterpret_cast<const uint4 *>(residual + static_cast<size_t>(t) * d);
     uint4 *hr = reinterpret_cast<uint4 *>(h_out + static_cast<size_t>(t) * d);
+    uint4 row[kRowUnits];
     float ss = 0.f;
-    for (int v = threadIdx.x; v < nunits; v += blockDim.x) {
+    auto make_h = [&](int v) -> uint4 {
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -529,17 +567,36 @@ __global__ void combine_residual_rmsnorm_kernel(const __nv_bfloat16 *__restrict_
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss = fmaf(yb[i], yb[i], ss);
         }
+        return hp;
+    };
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kRowUnits; ++i) {
+            const int v = threadIdx.x + i * nthr;
+            if (v < nunits) row[i] = make_h(v);
+        }
+    } else {
+        for (int v = threadIdx.x; v < nunits; v += nthr) make_h(v);
     }
     if (!gamma) return;   // uniform over the CTA
     const float inv = rms_inverse(block_sum(ss, red), d, eps);
     const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
-    for (int v = threadIdx.x; v < nunits; v += blockDim.x) {
+    auto emit = [&](int v, const uint4 &hp) {
         float hv[8], g[8];
-        unpack_bf16x8(hr[v], hv);
+        unpack_bf16x8(hp, hv);
         unpack_bf16x8(gr[v], g);
 #pragma unroll
         for (int i = 0; i < 8; ++i) hv[i] = hv[i] * inv * g[i];
         reinterpret_cast<uint4 *>(x_next + static_cast<size_t>(t) * d)[v] = pack_bf16x8(hv);
+    };
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kRowUnits; ++i) {
+            const int v = threadIdx.x + i * nthr;
+            if (v < nunits) emit(v, row[i]);
+        }
+    } else {
+        for (int v = threadIdx.x; v < nunits; v += nthr) emit(v, hr[v]);
     }
 }
 

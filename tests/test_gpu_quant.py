@@ -66,3 +66,47 @@ def test_e4m3_rounding_at_every_midpoint():
     qo, so = O.quantize_1x128(x)
     assert (so == 1.0).all()
     np.testing.assert_array_equal(q, qo)
+
+
+def _division_sweep(amax: np.ndarray) -> np.ndarray:
+    """One 128-group per group maximum: entry 0 is amax, entries 1..127 sweep
+    twelve binades below it (alternating signs), all bf16 values."""
+    j = np.arange(1, 128)
+    u = (1.0 + ((j * 37) % 128) / 128.0) / 2.0 * 2.0 ** -(j % 12)    # in (0, 1)
+    sign = np.where(j % 2 == 0, 1.0, -1.0)
+    g = np.empty((amax.size, 128), np.float64)
+    g[:, 0] = amax
+    g[:, 1:] = amax[:, None] * u[None, :] * sign[None, :]
+    return O.round_bf16(g).astype(np.float32)
+
+
+def test_quantiser_division_every_bf16_maximum():
+    # every positive normal bf16 value is the maximum of one group, so s = amax / 448
+    # takes all its values, and each group's codes depend on the correctly rounded
+    # x / s of 127 other entries: bit-exact against the oracle's IEEE fp32 division
+    e = np.arange(-126, 128)
+    m = np.arange(128)
+    amax = (np.ldexp(1.0 + m[None, :] / 128.0, e[:, None])).ravel()
+    amax = amax[amax < 3.3e38]
+    groups = _division_sweep(amax)
+    cols = 7168
+    pad = (-groups.shape[0]) % (cols // 128)
+    groups = np.concatenate([groups, np.zeros((pad, 128), np.float32)])
+    x = torch.from_numpy(groups.reshape(-1, cols)).to(torch.bfloat16)
+    q, s = _run(x)
+    qo, so = O.quantize_1x128(x.float().numpy())
+    np.testing.assert_array_equal(s.view(np.uint32), so.view(np.uint32))
+    np.testing.assert_array_equal(q, qo)
+
+
+def test_quantiser_division_subnormal_scales():
+    # group maxima below 448 * 2^-126 give subnormal scales, where the quantiser falls
+    # back to the plain division
+    amax = np.ldexp(1.0 + np.arange(0, 128, 8) / 128.0, -120)
+    groups = _division_sweep(amax)
+    x = torch.from_numpy(groups.reshape(-1, 2048)).to(torch.bfloat16)
+    q, s = _run(x)
+    qo, so = O.quantize_1x128(x.float().numpy())
+    assert (so < 1.17549435e-38).all()
+    np.testing.assert_array_equal(s.view(np.uint32), so.view(np.uint32))
+    np.testing.assert_array_equal(q, qo)
