@@ -208,6 +208,18 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// acc[i] += s * p[i], i < 16, as eight two-lane packed FMAs: each lane is an
+// ordinary fma.rn, so the sums equal fmaf's bit for bit with half the issue slots
+__device__ __forceinline__ void fold16(float *acc, const float *p, float s) {
+    const float2 s2 = make_float2(s, s);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float2 r = __ffma2_rn(s2, make_float2(p[i], p[i + 1]), make_float2(acc[i], acc[i + 1]));
+        acc[i] = r.x;
+        acc[i + 1] = r.y;
+    }
+}
+
 // Shared-memory carve-up of one CTA (offsets from a 1024-byte aligned base).
 template <Kind KIND, int BN> struct SmemLayout {
     using C = KindCfg<KIND, BN>;
@@ -246,6 +258,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     constexpr uint32_t kFmt = C::kBf16 ? 1u : 0u;
     constexpr int HC = C::kHalfCols;
     constexpr int kEpi = C::kEpiWarps;
+    // arrivals that release a partial buffer or a scale slot: one per epilogue warp,
+    // or one per epilogue thread in the 256-row kinds
+    constexpr int kRelease = C::kWide ? kEpi * 32 : kEpi;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -288,11 +303,11 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         }
         for (int s = 0; s < C::kScaleSlots; ++s) {
             mbar_init(smem_u32(&sfull[s]), 32);    // one cp.async arrival per scale-warp lane
-            mbar_init(smem_u32(&sempty[s]), kEpi); // one arrival per epilogue warp
+            mbar_init(smem_u32(&sempty[s]), kRelease);
         }
         for (int b = 0; b < C::kNumPart; ++b) {
             mbar_init(smem_u32(&pfull[b]), 1);
-            mbar_init(smem_u32(&pempty[b]), kEpi);
+            mbar_init(smem_u32(&pempty[b]), kRelease);
         }
         mbar_init(smem_u32(mma_done), 1);
         for (int b = 0; b < 2 * C::kGroups; ++b) mbar_init(smem_u32(&amax_bar[b]), 4);
@@ -604,16 +619,14 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                             tmem_ld16(tpart + chunk_col(c), p);
                             tmem_wait_ld();
                             const float s_c = (c < 2) ? s_lo : s_hi;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s_c, p[i], acc[c * 16 + i]);
+                            fold16(acc + c * 16, p, s_c);
                         }
                     }
+                    // every thread releases the partial and the scale slot itself: no
+                    // warp barrier and no single-lane branch in the K loop
                     tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(smem_u32(&pempty[pb]));
-                        mbar_arrive(smem_u32(&sempty[ss]));
-                    }
+                    mbar_arrive(smem_u32(&pempty[pb]));
+                    mbar_arrive(smem_u32(&sempty[ss]));
                 }
                 if (!ok) break;
                 const size_t row = static_cast<size_t>(I.row0 + r);
@@ -719,9 +732,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     const float s_kb = sc[BN] * sc[r];
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s_kb, p[c][i], acc[c * 16 + i]);
+                    for (int c = 0; c < C::kChunks; ++c) fold16(acc + c * 16, p[c], s_kb);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
