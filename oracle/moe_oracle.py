@@ -234,13 +234,19 @@ def swiglu_fp8(xq, xs, w1q, w1s, w3q, w3s, w2q, w2s):
     128x128 block scales. h = silu(g) * u is rounded to fp32 and quantised 1x128
     before the down projection. Returns (o fp64 [n, d], hq, hs).
     """
-    xh = dequantize_1x128(xq, xs)
-    g = xh @ decode_block_weight(w1q, w1s).T
-    u = xh @ decode_block_weight(w3q, w3s).T
-    h = (silu(g) * u).astype(np.float32)
+    h = swiglu_h(xq, xs, w1q, w1s, w3q, w3s)
     hq, hs = quantize_1x128(h)
     o = dequantize_1x128(hq, hs) @ decode_block_weight(w2q, w2s).T
     return o, hq, hs
+
+
+def swiglu_h(xq, xs, w1q, w1s, w3q, w3s):
+    """h = silu(gate x) * up x for rows of quantised activations, formed in fp64
+    and rounded to fp32: the value the 1x128 quantiser of the down input sees."""
+    xh = dequantize_1x128(xq, xs)
+    g = xh @ decode_block_weight(w1q, w1s).T
+    u = xh @ decode_block_weight(w3q, w3s).T
+    return (silu(g) * u).astype(np.float32)
 
 
 def _np(t):
