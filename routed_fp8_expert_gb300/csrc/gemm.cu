@@ -19,8 +19,7 @@ static cudaError_t launch_kind(const CUtensorMap &map_a, const ActMaps &map_b, c
     else kernel = grouped_gemm_kernel<KIND, BN>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kernel<<<grid, KindCfg<KIND, BN>::kThreads, smem, stream>>>(map_a, map_b, args);
-    return cudaGetLastError();
+    return launch_pdl(kernel, dim3(grid), dim3(KindCfg<KIND, BN>::kThreads), smem, stream, map_a, map_b, args);
 }
 
 // Token-tile widths compiled per kind: the swap-AB kinds serve decode-sized

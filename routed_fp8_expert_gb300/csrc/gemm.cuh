@@ -290,12 +290,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (args.single_rows < 0) {
-        for (int i = threadIdx.x; i <= args.G; i += blockDim.x) {
-            s_tp[i] = args.tile_prefix[i];
-            s_rs[i] = args.row_start[i];
-        }
-    }
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);    // the producer's expect_tx arrival (+ TMA bytes)
@@ -321,6 +316,15 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         for (int i = 0; i < kActBoxes; ++i) tma_prefetch_desc(&map_b.box[i]);
     }
     if (warp == 1) tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
+    // the set-up above touches only shared memory, TMEM and the kernel's parameters,
+    // so it overlaps the preceding kernel's tail; the global inputs come after it
+    pdl_wait();
+    if (args.single_rows < 0) {
+        for (int i = threadIdx.x; i <= args.G; i += blockDim.x) {
+            s_tp[i] = args.tile_prefix[i];
+            s_rs[i] = args.row_start[i];
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace moe {
 
@@ -16,6 +17,26 @@ constexpr int kActBoxes = 5;
 struct ActMaps {
     CUtensorMap box[kActBoxes];
 };
+
+// Launches `kernel` on `stream` with programmatic dependent launch allowed: its
+// CTAs may be scheduled while the stream's preceding kernel finishes. Every kernel
+// of the library starts with pdl_trigger() and calls pdl_wait() before its first
+// global-memory access, so the stream order of all memory effects is kept.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Grouped tcgen05 GEMM launch (gemm.cu). Returns a cudaError_t.
 cudaError_t launch_grouped_gemm(Kind kind, int bn, const CUtensorMap &map_a, const ActMaps &map_b,

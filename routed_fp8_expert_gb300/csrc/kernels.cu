@@ -12,18 +12,19 @@ cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint
     int64_t blocks = (groups + 7) / 8;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
+    const int st = s_transposed ? 1 : 0;
     if (bf16)
-        quant_1x128_kernel<true><<<static_cast<int>(blocks), threads, 0, stream>>>(in, rows, cols, q, s, s_transposed);
-    else
-        quant_1x128_kernel<false><<<static_cast<int>(blocks), threads, 0, stream>>>(in, rows, cols, q, s, s_transposed);
-    return cudaGetLastError();
+        return launch_pdl(quant_1x128_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, in,
+                          rows, cols, q, s, st);
+    return launch_pdl(quant_1x128_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, in,
+                      rows, cols, q, s, st);
 }
 
 cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream) {
     const int threads = 64;   // 2 tokens per block: a 256-token batch spreads over 128 blocks
-    topk_kernel<<<(T + 1) / 2, threads, 0, stream>>>(logits, splits, bias, T, E, k, scale, idx, w, scores);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3((T + 1) / 2), dim3(threads), 0, stream, logits, splits, bias, T, E, k, scale,
+                      idx, w, scores);
 }
 
 cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *sx, int T, int k, int S, int E,
@@ -34,24 +35,26 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
                            cudaStream_t stream) {
     const int C = (T + 31) / 32;
     const size_t smem = sizeof(uint32_t) * kPermWarps * E;
-    perm_rank_kernel<<<(C + kPermWarps - 1) / kPermWarps, kPermWarps * 32, smem, stream>>>(idx, T, k, E, C, rank,
-                                                                                            cnt);
-    perm_scan_kernel<<<E, 256, 0, stream>>>(cnt, C, counts);
-    perm_offsets_kernel<<<1, 1024, 0, stream>>>(counts, E, S, T, k, tile_a, tile_b, offsets, row_start,
-                                                tile_prefix_a, tile_prefix_b, counters);
+    cudaError_t e = launch_pdl(perm_rank_kernel, dim3((C + kPermWarps - 1) / kPermWarps), dim3(kPermWarps * 32), smem,
+                               stream, idx, T, k, E, C, rank, cnt);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(perm_scan_kernel, dim3(E), dim3(256), 0, stream, cnt, C, counts);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(perm_offsets_kernel, dim3(1), dim3(1024), 0, stream, counts, E, S, T, k, tile_a, tile_b, offsets,
+                   row_start, tile_prefix_a, tile_prefix_b, counters);
+    if (e != cudaSuccess) return e;
     const int threads = min(1024, max(64, d / 16));
-    perm_scatter_kernel<<<T, threads, 0, stream>>>(idx, rank, cnt, offsets, xq, sx, T, k, S, E, d, C, sorted_tok,
-                                                   inv_pos, xq_perm, sx_perm);
+    e = launch_pdl(perm_scatter_kernel, dim3(T), dim3(threads), 0, stream, idx, rank, cnt, offsets, xq, sx, T, k, S,
+                   E, d, C, sorted_tok, inv_pos, xq_perm, sx_perm);
     *launches += 4;
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
                          int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b, int32_t *counters,
                          cudaStream_t stream) {
-    sched_kernel<<<1, 1024, 0, stream>>>(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a,
-                                         tile_prefix_b, counters);
-    return cudaGetLastError();
+    return launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, stream, offsets, E, S, T, k, tile_a, tile_b, row_start,
+                      tile_prefix_a, tile_prefix_b, counters);
 }
 
 cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos, int T, int k, int S, int d,
@@ -60,9 +63,8 @@ cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos
     const int units = d / 8;
     const int threads = 128;
     const dim3 grid(T, (units + threads - 1) / threads);
-    combine_kernel<<<grid, threads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d,
-                                                 static_cast<__nv_bfloat16 *>(y));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(threads), 0, stream, static_cast<const __nv_bfloat16 *>(o), w,
+                      inv_pos, T, k, S, d, static_cast<__nv_bfloat16 *>(y));
 }
 
 // Threads of a one-row-per-CTA kernel: kRowUnits 8-element units each, a multiple
@@ -75,20 +77,18 @@ static int row_threads(int cols) {
 
 cudaError_t launch_rmsnorm_quant(const void *h, const void *gamma, float eps, int rows, int cols, void *y,
                                  uint8_t *q, float *s, bool s_transposed, cudaStream_t stream) {
-    rmsnorm_quant_kernel<<<rows, row_threads(cols), 0, stream>>>(static_cast<const __nv_bfloat16 *>(h),
-                                                    static_cast<const __nv_bfloat16 *>(gamma), eps, cols,
-                                                    static_cast<__nv_bfloat16 *>(y), q, s, rows, s_transposed ? 1 : 0);
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_quant_kernel, dim3(rows), dim3(row_threads(cols)), 0, stream,
+                      static_cast<const __nv_bfloat16 *>(h), static_cast<const __nv_bfloat16 *>(gamma), eps, cols,
+                      static_cast<__nv_bfloat16 *>(y), q, s, rows, s_transposed ? 1 : 0);
 }
 
 cudaError_t launch_combine_residual_rmsnorm(const void *o, const float *w, const int32_t *inv_pos, int T, int k,
                                             int S, int d, const void *residual, const void *gamma, float eps,
                                             void *h_out, void *x_next, cudaStream_t stream) {
-    combine_residual_rmsnorm_kernel<<<T, row_threads(d), 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d, static_cast<const __nv_bfloat16 *>(residual),
-        static_cast<const __nv_bfloat16 *>(gamma), eps, static_cast<__nv_bfloat16 *>(h_out),
-        static_cast<__nv_bfloat16 *>(x_next));
-    return cudaGetLastError();
+    return launch_pdl(combine_residual_rmsnorm_kernel, dim3(T), dim3(row_threads(d)), 0, stream,
+                      static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T, k, S, d,
+                      static_cast<const __nv_bfloat16 *>(residual), static_cast<const __nv_bfloat16 *>(gamma), eps,
+                      static_cast<__nv_bfloat16 *>(h_out), static_cast<__nv_bfloat16 *>(x_next));
 }
 
 }  // namespace moe

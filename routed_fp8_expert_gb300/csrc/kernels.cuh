@@ -25,6 +25,8 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&v)[8]) {
 template <bool kBf16In>
 __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, int cols,
                                    uint8_t *__restrict__ q, float *__restrict__ s, int s_transposed) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int gpr = cols / 128;
     const int64_t n_groups = rows * gpr;
@@ -67,6 +69,8 @@ __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, in
 __global__ void topk_kernel(const float *__restrict__ logits, int splits, const float *__restrict__ bias,
                             int T, int E, int k, float route_scale, int32_t *__restrict__ topk_idx,
                             float *__restrict__ topk_w, float *__restrict__ scores) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
@@ -145,6 +149,8 @@ constexpr int kPermWarps = 8;
 // Ids outside [0, E) are skipped (rank -1), so bad input cannot write out of bounds.
 __global__ void perm_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int C,
                                  int32_t *__restrict__ rank, int32_t *__restrict__ cnt) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ uint32_t s_bits[];  // [kPermWarps][E]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x * kPermWarps + warp;
@@ -174,6 +180,8 @@ __global__ void perm_rank_kernel(const int32_t *__restrict__ idx, int T, int k, 
 
 // Exclusive scan of one expert's per-chunk counts (in place); total -> counts[e].
 __global__ void perm_scan_kernel(int32_t *__restrict__ cnt, int C, int32_t *__restrict__ counts) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t s_warp[32];
     __shared__ int32_t s_carry;
     const int e = blockIdx.x;
@@ -290,6 +298,8 @@ __global__ void perm_offsets_kernel(const int32_t *__restrict__ counts, int E, i
                                     int tile_b, int32_t *__restrict__ offsets, int32_t *__restrict__ row_start,
                                     int32_t *__restrict__ tile_prefix_a, int32_t *__restrict__ tile_prefix_b,
                                     int32_t *__restrict__ counters) {
+    pdl_trigger();
+    pdl_wait();
     block_exclusive_scan<1>(counts, E, offsets, offsets + E);
     schedule_block(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a, tile_prefix_b, counters);
 }
@@ -297,6 +307,8 @@ __global__ void perm_offsets_kernel(const int32_t *__restrict__ counts, int E, i
 __global__ void sched_kernel(const int32_t *__restrict__ offsets, int E, int S, int T, int k, int tile_a, int tile_b,
                              int32_t *__restrict__ row_start, int32_t *__restrict__ tile_prefix_a,
                              int32_t *__restrict__ tile_prefix_b, int32_t *__restrict__ counters) {
+    pdl_trigger();
+    pdl_wait();
     schedule_block(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a, tile_prefix_b, counters);
 }
 
@@ -309,6 +321,8 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
                                     int S, int E, int d, int C, int32_t *__restrict__ sorted_tok,
                                     int32_t *__restrict__ inv_pos, uint8_t *__restrict__ xq_perm,
                                     float *__restrict__ sx_perm) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t s_pos[40];
     const int t = blockIdx.x;
     const int c = t >> 5;
@@ -351,6 +365,8 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
 __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w,
                                const int32_t *__restrict__ inv_pos, int T, int k, int S, int d,
                                __nv_bfloat16 *__restrict__ y) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t s_pos[32];
     __shared__ float s_w[32];
     const int t = blockIdx.x;
@@ -442,6 +458,8 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const __nv_bfloat16
                                                              int cols, __nv_bfloat16 *__restrict__ y,
                                                              uint8_t *__restrict__ q, float *__restrict__ s, int rows,
                                                              int s_transposed) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[33];
     const int r = blockIdx.x;
     const int lane = threadIdx.x & 31;
@@ -521,6 +539,8 @@ __global__ void __launch_bounds__(1024) combine_residual_rmsnorm_kernel(
     const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w, const int32_t *__restrict__ inv_pos, int T,
     int k, int S, int d, const __nv_bfloat16 *__restrict__ residual, const __nv_bfloat16 *__restrict__ gamma,
     float eps, __nv_bfloat16 *__restrict__ h_out, __nv_bfloat16 *__restrict__ x_next) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t s_pos[32];
     __shared__ float s_w[32];
     __shared__ float red[33];

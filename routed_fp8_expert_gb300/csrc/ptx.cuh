@@ -24,6 +24,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch. pdl_trigger lets the next kernel of the stream
+// start launching (its CTAs take free SM resources and wait); pdl_wait blocks until
+// the preceding kernel of the stream has completed and its memory is visible. Both
+// are no-ops for a kernel launched without the programmatic-serialisation attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
