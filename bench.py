@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Throughput of the routed FP8 MoE FFN layer forward (Kimi K2 shapes) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|dense]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|skewed40|dense]
                     [--impl ours|reference]
 
 One step = one forward of the whole layer over one batch of T tokens already
@@ -48,10 +48,12 @@ DECODE_E64 = S.MoEShape("kimi_k2_moe_decode_e64_t48", T=48, d=7168, E=64, topk=8
 # prefill_e64: 64 routed experts and 768 tokens (96 rows per expert, the 128-token
 # tile path of the prefill batch; 2.9 GB of weights)
 PREFILL_E64 = S.MoEShape("kimi_k2_moe_prefill_e64_t768", T=768, d=7168, E=64, topk=8, H=2048)
-WORKLOADS = {"decode": S.DECODE, "prefill": S.PREFILL, "skewed": S.SKEWED, "dense": S.DENSE, "toy": S.TOY,
+WORKLOADS = {"decode": S.DECODE, "prefill": S.PREFILL, "skewed": S.SKEWED, "skewed40": S.SKEWED40,
+             "dense": S.DENSE, "toy": S.TOY,
              "decode_e64": DECODE_E64, "prefill_e64": PREFILL_E64}
 DATA = ("synthetic, seeded: x ~ N(0,1) bf16; W_g ~ N(0,0.02) bf16; bias ~ N(0,0.01) fp32 (+0.5 on 16 hot "
-        "experts for the skewed workload); expert weights ~ N(0,0.02) stored e4m3 with 128x128 fp32 scales")
+        "experts for the skewed workload, +0.18 for skewed40); expert weights ~ N(0,0.02) stored e4m3 with "
+        "128x128 fp32 scales")
 
 # DRAM bytes (read + write) per launch of the decode gate/up kernel, from one ncu
 # capture of the same kernel on the decode-like case of a few GB (decode_e64:
@@ -59,7 +61,7 @@ DATA = ("synthetic, seeded: x ~ N(0,1) bf16; W_g ~ N(0,0.02) bf16; bias ~ N(0,0.
 # the touched experts' weights, so the full launch's figure is this ratio times
 # its algorithmic bytes. Keyed by the hash of the kernel sources at capture
 # time: once the sources change, the figure no longer applies (null).
-NCU_TRAFFIC = {"ratio": 1.0017, "src": "514e7d5b95942272", "case": "decode_e64"}
+NCU_TRAFFIC = {"ratio": 1.0017, "src": "a094e19cbc7dfc06", "case": "decode_e64"}
 
 
 def kernel_src_hash() -> str:
@@ -437,6 +439,8 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
                   (layer_weight_bytes + 2 * T * d * 2) / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
                   "tflops": flops / (ms_step * 1e-3) / 1e12, "fp8_peak_tflops": 2 * peaks["bf16_tflops"],
                   "touched_experts": touched, "max_rows_per_expert": int(counts.max()),
+                  **({"hot_share": float(counts[list(shape.hot_experts)].sum() / counts[:E].sum())}
+                     if shape.hot_experts else {}),
                   "kernels_ms": per},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * d * 2,
                 "d2h_bytes_per_step": T * d * 2, "api": "moe_layer_forward", "matches_step_output": bool(same)},

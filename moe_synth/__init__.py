@@ -59,16 +59,20 @@ def _hot(E: int, n: int) -> tuple:
     return tuple(i * step for i in range(n))
 
 
-# The five workloads: a toy layer the oracle runs in seconds, then the Kimi K2
-# layer at decode, prefill and skewed-routing batches, then the dense FFN.
+# The workloads: a toy layer the oracle runs in seconds, then the Kimi K2 layer at
+# decode, prefill and two skewed-routing batches, then the dense FFN.
 TOY = MoEShape("toy_t64_d1024_e32_h256", T=64, d=1024, E=32, topk=8, H=256)
 DECODE = MoEShape("kimi_k2_moe_decode_t256", T=256, d=7168, E=384, topk=8, H=2048)
 PREFILL = MoEShape("kimi_k2_moe_prefill_t4096", T=4096, d=7168, E=384, topk=8, H=2048)
 SKEWED = MoEShape("kimi_k2_moe_skewed_t16384", T=16384, d=7168, E=384, topk=8, H=2048,
                   hot_experts=_hot(384, 16), hot_bias=0.5)
+# the same mechanism with the bias that gives the hot experts about 40% of the
+# routed assignments under these distributions (+0.5 gives about 90%)
+SKEWED40 = MoEShape("kimi_k2_moe_skewed40_t16384", T=16384, d=7168, E=384, topk=8, H=2048,
+                    hot_experts=_hot(384, 16), hot_bias=0.18)
 DENSE = DenseShape("kimi_k2_dense_ffn_t8192", T=8192, d=7168, H=18432)
 
-SHAPES = {s.name: s for s in (TOY, DECODE, PREFILL, SKEWED)}
+SHAPES = {s.name: s for s in (TOY, DECODE, PREFILL, SKEWED, SKEWED40)}
 
 
 def sub_seed(seed: int, name: str, idx: int = 0) -> int:

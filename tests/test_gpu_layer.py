@@ -87,7 +87,11 @@ def _kimi(shape, ex_dev, n_tokens, seed=0):
     assert_close_layer(y.cpu()[toks], ref["y"][toks], what=shape.name)
     # permutation-level invariants over all tokens
     np.testing.assert_allclose(w.cpu().numpy().sum(1), shape.route_scale, rtol=1e-5)
-    return y
+    return y, use_idx
+
+
+def _hot_share(shape, idx):
+    return float(np.isin(idx, shape.hot_experts).mean())
 
 
 def test_kimi_decode_layer_sampled(kimi_weights):
@@ -102,5 +106,14 @@ def test_kimi_skewed_layer_sampled(kimi_weights):
     # the skewed batch (T=16384, +0.5 bias on 16 hot experts): the hot experts hold
     # thousands of rows each, so dozens of 128-token tiles share every weight block
     # and the dynamic scheduler hands them out
-    y = _kimi(S.SKEWED, kimi_weights, n_tokens=3, seed=2)
+    y, idx = _kimi(S.SKEWED, kimi_weights, n_tokens=3, seed=2)
     assert torch.isfinite(y.float()).all()
+    # the stated +0.5 bias gives the 16 hot experts about nine tenths of the assignments
+    assert _hot_share(S.SKEWED, idx) > 0.8
+
+
+def test_kimi_skewed40_layer_sampled(kimi_weights):
+    # the same mechanism at +0.18, the bias that gives the hot experts about 40%
+    y, idx = _kimi(S.SKEWED40, kimi_weights, n_tokens=3, seed=3)
+    assert torch.isfinite(y.float()).all()
+    assert 0.3 < _hot_share(S.SKEWED40, idx) < 0.5
