@@ -380,24 +380,42 @@ __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float 
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    // the routed slots' rows are loaded a batch at a time before any of them is
+    // added, so their loads are in flight together; the sums keep the fixed order
+    // (shared experts, then slots j = 0, 1, ...)
+    constexpr int kBatch = 8;
+    uint4 raw[kBatch];
+    auto load_batch = [&](int j0) {
+#pragma unroll
+        for (int jj = 0; jj < kBatch; ++jj) {
+            const int j = j0 + jj;
+            raw[jj] = make_uint4(0u, 0u, 0u, 0u);
+            if (j < k && s_pos[j] >= 0) raw[jj] = reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v];
+        }
+    };
+    load_batch(0);
     for (int s = 0; s < S; ++s) {
-        const uint4 raw = reinterpret_cast<const uint4 *>(o + (static_cast<size_t>(k) * T + static_cast<size_t>(s) * T + t) * d)[v];
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+        const uint4 rs = reinterpret_cast<const uint4 *>(o + (static_cast<size_t>(k) * T + static_cast<size_t>(s) * T + t) * d)[v];
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&rs);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             acc[2 * i] += __low2float(h[i]);
             acc[2 * i + 1] += __high2float(h[i]);
         }
     }
-    for (int j = 0; j < k; ++j) {
-        if (s_pos[j] < 0) continue;
-        const uint4 raw = reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v];
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-        const float wj = s_w[j];
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+        if (j0 > 0) load_batch(j0);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(wj, __low2float(h[i]), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(wj, __high2float(h[i]), acc[2 * i + 1]);
+        for (int jj = 0; jj < kBatch; ++jj) {
+            const int j = j0 + jj;
+            if (j >= k || s_pos[j] < 0) continue;
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw[jj]);
+            const float wj = s_w[j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj, __low2float(h[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, __high2float(h[i]), acc[2 * i + 1]);
+            }
         }
     }
     uint4 out;
