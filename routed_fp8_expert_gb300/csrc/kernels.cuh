@@ -553,7 +553,13 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const __nv_bfloat16
 // output), plus the block's residual addition h = bf16(residual + y), and, when
 // gamma is given, the next block's input RMSNorm x = bf16(h * inv * gamma) of that
 // bf16 row. One CTA per token; thread t holds units t + i * blockDim as above.
-__global__ void __launch_bounds__(1024) combine_residual_rmsnorm_kernel(
+// kBatch: load a token's routed rows eight slots at a time (more loads in flight
+// per thread, for batches too small to fill the GPU with CTAs); it needs rows of
+// at most 256 threads (d <= 8192), for the register room (up to 128 a thread).
+// Without it the launch bound is 1024 threads and 64 registers, for the occupancy
+// that large batches want.
+template <bool kBatch>
+__global__ void __launch_bounds__(kBatch ? 256 : 1024, kBatch ? 2 : 1) combine_residual_rmsnorm_kernel(
     const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w, const int32_t *__restrict__ inv_pos, int T,
     int k, int S, int d, const __nv_bfloat16 *__restrict__ residual, const __nv_bfloat16 *__restrict__ gamma,
     float eps, __nv_bfloat16 *__restrict__ h_out, __nv_bfloat16 *__restrict__ x_next) {
@@ -585,13 +591,38 @@ __global__ void __launch_bounds__(1024) combine_residual_rmsnorm_kernel(
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] += e[i];
         }
-        for (int j = 0; j < k; ++j) {
-            if (s_pos[j] < 0) continue;
-            float e[8];
-            unpack_bf16x8(reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v], e);
-            const float wj = s_w[j];
+        if constexpr (kBatch) {
+            // the rows of eight slots are loaded before they are added; the order of
+            // the sums is that of combine_kernel
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                uint4 raw[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, e[i], acc[i]);
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = j0 + jj;
+                    raw[jj] = make_uint4(0u, 0u, 0u, 0u);
+                    if (j < k && s_pos[j] >= 0)
+                        raw[jj] = reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v];
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = j0 + jj;
+                    if (j >= k || s_pos[j] < 0) continue;
+                    float e[8];
+                    unpack_bf16x8(raw[jj], e);
+                    const float wj = s_w[j];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, e[i], acc[i]);
+                }
+            }
+        } else {
+            for (int j = 0; j < k; ++j) {
+                if (s_pos[j] < 0) continue;
+                float e[8];
+                unpack_bf16x8(reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v], e);
+                const float wj = s_w[j];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, e[i], acc[i]);
+            }
         }
         float yb[8], res[8];
         unpack_bf16x8(pack_bf16x8(acc), yb);   // the FFN output is a bf16 tensor

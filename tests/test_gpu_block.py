@@ -82,7 +82,8 @@ def _combine_case(T, d, E, k, seed):
     return idx, p, o, w, res, g
 
 
-@pytest.mark.parametrize("T,d", [(1, 128), (48, 1024), (33, 7168)])
+# T > 512 takes the 64-register variant (no batched row loads)
+@pytest.mark.parametrize("T,d", [(1, 128), (48, 1024), (33, 7168), (600, 1024)])
 def test_combine_residual_rmsnorm(T, d):
     E, k = 16, 4
     idx, p, o, w, res, g = _combine_case(T, d, E, k, seed=T + 1)
@@ -108,8 +109,11 @@ def test_combine_residual_rmsnorm(T, d):
     if diff.any():
         bound = _ulp_bf16(O.round_bf16(y_ref))[diff] + _ulp_bf16(h_ref)[diff]
         assert (np.abs(got_h - h_ref)[diff] <= bound * (1 + 1e-9)).all()
-    x_ref = O.rms_norm(h_ref, g, EPS)
-    _near_bf16(x_next.float().cpu().numpy().astype(np.float64), x_ref, "x_next", ulps=2.0, max_frac=5e-3)
+    # the next block's RMSNorm, given the same h: the oracle's rms_norm of the GPU's own
+    # h_out (an h that differs by one ulp can move x by more than two ulps of x where
+    # the product crosses a binade, so the stages are checked one at a time)
+    x_ref = O.rms_norm(got_h, g, EPS)
+    _near_bf16(x_next.float().cpu().numpy().astype(np.float64), x_ref, "x_next", ulps=1.0)
     # without the norm: the same h, no x
     h2, none = moe.combine_residual_rmsnorm(o.to(DEV), w.to(DEV), inv.to(DEV), cfg, T, res.to(DEV))
     assert none is None
