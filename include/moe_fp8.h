@@ -19,7 +19,13 @@
  *    except `cfg` (host). The library never allocates or frees and never
  *    synchronises the stream. Device buffers must be 16-byte aligned.
  *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream). Every
- *    call only enqueues work on it and returns.
+ *    call only enqueues work on it and returns. The kernels are launched with
+ *    programmatic dependent launch allowed: each waits for the stream's
+ *    preceding kernel to complete before it touches global memory, and lets
+ *    the next kernel start launching at once. Ordinary launches, copies and
+ *    events after a call keep plain stream order. A kernel the caller launches
+ *    after a call with the programmatic-serialisation attribute must itself
+ *    wait (cudaGridDependencySynchronize) before it reads the call's outputs.
  *  - Errors: every call returns a moe_status_t. Arguments are checked on the
  *    host before anything is enqueued; on an error nothing is enqueued.
  *    moe_last_error_string() describes the last error of the calling thread.
