@@ -56,6 +56,11 @@ namespace moe {
 // DownWide: token-major down projection with two adjacent 128-row blocks (N = 256).
 enum class Kind { GateUp, Down, Router, DownPair, GateUpWide, DownWide };
 
+// Column groups of the 256-row token-major kinds' epilogue: 2 gives eight epilogue
+// warps of 128 accumulators a thread (eleven warps, 168 registers a thread), 4
+// gives sixteen warps of 64 (nineteen warps, 96 registers).
+constexpr int kWideGroups = 2;
+
 constexpr int kBM = 128;                    // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // bytes of K per stage (= one swizzle row)
 constexpr int kATileBytes = kBM * kKBytes;  // 16 KB
@@ -94,15 +99,21 @@ template <Kind K, int BN> struct KindCfg {
     // are released by the MMA alone and the producer keeps kStages ahead of it
     static constexpr int kScaleSlots = kPromote ? (kStages + kNumPart + 2) : 1;
     // epilogue column groups: token columns (swap-AB) or weight rows (token-major);
-    // four for the 256-row items, so that each thread holds 64 accumulators
-    static constexpr int kGroups = kWide ? 4 : 2;
-    static constexpr int kHalfCols = kWide ? 64 : (kTM ? kBM : BN) / kGroups;  // accumulators per thread
+    // kWideGroups for the 256-row items, each thread holding 256 / kWideGroups
+    // accumulators
+    static constexpr int kGroups = kWide ? kWideGroups : 2;
+    static constexpr int kHalfCols = kWide ? 256 / kWideGroups : (kTM ? kBM : BN) / kGroups;  // accumulators per thread
     static constexpr int kChunks = kHalfCols / 16;
     static constexpr int kEpiWarps = 4 * kGroups;                 // one warp per TMEM lane quarter and group
     // the K blocks' scales are copied by a warp of their own, beside the producer
     static constexpr bool kScaleWarpOwn = kPromote;
     static constexpr int kScaleWarp = 2 + kEpiWarps;
     static constexpr int kThreads = 64 + 32 * kEpiWarps + (kScaleWarpOwn ? 32 : 0);
+    // h amax exchange barriers: GateUp [groups][2 buffers]; wide [4 lane quarters][2]
+    static constexpr int kAmaxBars = kWide ? 8 : 2 * kGroups;
+    // registers a thread of the wide kinds may use: the register file is split over
+    // the four sub-partitions (16,384 each), which hold the CTA's warps round-robin
+    static constexpr int kWideRegs = (16384 / ((kThreads / 32 + 3) / 4 * 32)) / 8 * 8;
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
     static_assert(!kTM || BN == 128, "token-major tiles hold 128 tokens (the MMA M dimension)");
     static_assert(kStages * kKPS >= 4 && kStages >= 2, "pipeline depth");
@@ -223,7 +234,7 @@ __device__ __forceinline__ void fold16(float *acc, const float *p, float s) {
 // Shared-memory carve-up of one CTA (offsets from a 1024-byte aligned base).
 template <Kind KIND, int BN> struct SmemLayout {
     using C = KindCfg<KIND, BN>;
-    static constexpr int kNumBars = 2 * C::kStages + 2 * C::kNumPart + 1 + 2 * C::kGroups + 2 * kItemQ +
+    static constexpr int kNumBars = 2 * C::kStages + 2 * C::kNumPart + 1 + C::kAmaxBars + 2 * kItemQ +
                                     2 * C::kScaleSlots;
     static constexpr size_t kBars = static_cast<size_t>(C::kStages) * C::kStageBytes;
     static constexpr size_t kMisc = (kBars + kNumBars * 8 + 15) & ~size_t(15);
@@ -238,9 +249,10 @@ template <Kind KIND, int BN> struct SmemLayout {
     static constexpr size_t kAmaxBytes = (KIND == Kind::GateUp)       ? C::kGroups * 2 * 4 * C::kHalfCols * 4
                                          : (KIND == Kind::GateUpWide) ? 2 * 4 * kBM * 4
                                                                       : 0;
-    // DownWide: one 1 KB slot per epilogue warp to turn its rows into whole-line stores
+    // DownWide: a slot of eight output rows per epilogue warp to turn its rows into
+    // whole-line stores
     static constexpr size_t kXpose = kAmax + kAmaxBytes;
-    static constexpr size_t kEnd = kXpose + ((KIND == Kind::DownWide) ? C::kEpiWarps * 1024 : 0);
+    static constexpr size_t kEnd = kXpose + ((KIND == Kind::DownWide) ? C::kEpiWarps * 8 * C::kHalfCols * 2 : 0);
     static constexpr size_t kLaunchBytes = kEnd + 1024;  // + alignment slack of the dynamic base
     static_assert(kBars % 1024 == 0 && kScale % 16 == 0 && kCs % 16 == 0 && kXpose % 16 == 0, "alignment");
     static_assert(kLaunchBytes <= 232448, "shared memory budget");
@@ -271,8 +283,8 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     uint64_t *pfull = empty + C::kStages;
     uint64_t *pempty = pfull + C::kNumPart;
     uint64_t *mma_done = pempty + C::kNumPart;
-    uint64_t *amax_bar = mma_done + 1;                  // [groups][2 buffers]
-    uint64_t *item_full = amax_bar + 2 * C::kGroups;     // [kItemQ]
+    uint64_t *amax_bar = mma_done + 1;                  // [kAmaxBars]
+    uint64_t *item_full = amax_bar + C::kAmaxBars;       // [kItemQ]
     uint64_t *item_empty = item_full + kItemQ;           // [kItemQ]
     uint64_t *sfull = item_empty + kItemQ;               // [kScaleSlots]
     uint64_t *sempty = sfull + C::kScaleSlots;           // [kScaleSlots]
@@ -305,7 +317,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             mbar_init(smem_u32(&pempty[b]), kRelease);
         }
         mbar_init(smem_u32(mma_done), 1);
-        for (int b = 0; b < 2 * C::kGroups; ++b) mbar_init(smem_u32(&amax_bar[b]), 4);
+        for (int b = 0; b < C::kAmaxBars; ++b) mbar_init(smem_u32(&amax_bar[b]), C::kWide ? C::kGroups : 4);
         for (int b = 0; b < kItemQ; ++b) {
             mbar_init(smem_u32(&item_full[b]), 1);
             mbar_init(smem_u32(&item_empty[b]), 1 + kEpi + (C::kScaleWarpOwn ? 1 : 0));
@@ -575,18 +587,21 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
             const int n_my = max(0, min(HC, I.n - col_base));
             if constexpr (C::kWide) {
-                // token-major, 256 weight rows: thread = token row r; its 64 accumulators are
-                //   GateUpWide: gate [0, 32) and up [32, 64) of features 32*grp .. 32*grp+31
-                //   DownWide:   the 64 output rows 64*grp .. of the item's 256
+                // token-major, 256 weight rows: thread = token row r; its HC accumulators are
+                //   GateUpWide: gate [0, FPT) and up [FPT, HC) of features FPT*grp ..
+                //   DownWide:   the HC output rows HC*grp .. of the item's 256
+                constexpr int FPT = HC / 2;          // GateUpWide: features per thread
+                constexpr int kHalfChunks = C::kChunks / 2;
                 const int r = quad * 32 + lane;
                 const bool quad_live = quad * 32 < I.n;   // warp-uniform
                 float acc[HC];
 #pragma unroll
                 for (int j = 0; j < HC; ++j) acc[j] = 0.f;
-                // TMEM column of 16-column chunk c (0..3) inside a partial buffer
+                // TMEM column of 16-column chunk c inside a partial buffer
                 auto chunk_col = [&](int c) -> uint32_t {
-                    if constexpr (KIND == Kind::GateUpWide) return (c >> 1) * kBM + grp * 32 + (c & 1) * 16;
-                    else return grp * 64 + c * 16;
+                    if constexpr (KIND == Kind::GateUpWide)
+                        return (c / kHalfChunks) * kBM + grp * FPT + (c % kHalfChunks) * 16;
+                    else return grp * HC + c * 16;
                 };
                 // the partial ring and the scale ring advance together, one entry per K
                 // block, so one counter gives both positions
@@ -607,22 +622,22 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                         s_lo = sc[BN] * sx;       // gate block
                         s_hi = sc[BN + 1] * sx;   // up block
                     } else {
-                        s_lo = sc[BN + (grp >> 1)] * sx;
+                        s_lo = sc[BN + ((grp * HC) >> 7)] * sx;   // the group's 128-row block
                         s_hi = s_lo;
                     }
                     if (!mbar_wait(smem_u32(&pfull[pb]), pph, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t tpart = t_lane + pb * C::kPartCols;
                     float p[16];
-                    // one 16-column chunk in flight at a time (the 64 accumulators and
-                    // 16 partials fill the registers of the 19-warp CTA); a lane quarter
-                    // wholly past the tile's last token has nothing to fold
+                    // one 16-column chunk in flight at a time (the accumulators and 16
+                    // partials fill the thread's registers); a lane quarter wholly past
+                    // the tile's last token has nothing to fold
                     if (quad_live) {
 #pragma unroll
                         for (int c = 0; c < C::kChunks; ++c) {
                             tmem_ld16(tpart + chunk_col(c), p);
                             tmem_wait_ld();
-                            const float s_c = (c < 2) ? s_lo : s_hi;
+                            const float s_c = (c < kHalfChunks) ? s_lo : s_hi;
                             fold16(acc + c * 16, p, s_c);
                         }
                     }
@@ -635,9 +650,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 if (!ok) break;
                 const size_t row = static_cast<size_t>(I.row0 + r);
                 if constexpr (KIND == Kind::GateUpWide) {
-                    // h = silu(g) * u for the token's 32 features, then the 1x128 amax
-                    // over the block's 128 features, held by the four column-group
-                    // warps of this lane quarter: exchanged through shared memory
+                    // h = silu(g) * u for the token's FPT features, then the 1x128 amax
+                    // over the block's 128 features, held by the column-group warps of
+                    // this lane quarter: exchanged through shared memory
                     const int H = args.num_mb * kBM;
                     const int buf = item_count & 1;
                     const uint32_t ab = smem_u32(&amax_bar[quad * 2 + buf]);
@@ -645,8 +660,8 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     float am = 0.f;
                     if (quad_live) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            acc[j] = silu_f(acc[j]) * acc[32 + j];
+                        for (int j = 0; j < FPT; ++j) {
+                            acc[j] = silu_f(acc[j]) * acc[FPT + j];
                             am = fmaxf(am, fabsf(acc[j]));
                         }
                     }
@@ -655,28 +670,31 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     if (lane == 0) mbar_arrive(ab);
                     if (!mbar_wait(ab, (item_count >> 1) & 1, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
                     if (r < I.n) {
-                        const float amax = fmaxf(fmaxf(xch[r], xch[kBM + r]), fmaxf(xch[2 * kBM + r], xch[3 * kBM + r]));
+                        float amax = xch[r];
+#pragma unroll
+                        for (int g = 1; g < C::kGroups; ++g) amax = fmaxf(amax, xch[g * kBM + r]);
                         const float sq = amax / 448.0f;
                         // codes in feature order, four to a word (the first in the low byte);
                         // an all-zero group has scale 0 and codes 0
-                        uint32_t w[8];
+                        uint32_t w[FPT / 4];
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
+                        for (int v = 0; v < FPT / 4; ++v) {
                             const uint32_t lo = e4m3x2(acc[4 * v] / sq, acc[4 * v + 1] / sq);
                             const uint32_t hi = e4m3x2(acc[4 * v + 2] / sq, acc[4 * v + 3] / sq);
                             w[v] = (amax == 0.f) ? 0u : (lo | (hi << 16));
                         }
-                        uint4 *h4 = reinterpret_cast<uint4 *>(args.hq + row * H + I.mb * kBM + grp * 32);
-                        h4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        h4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        uint4 *h4 = reinterpret_cast<uint4 *>(args.hq + row * H + I.mb * kBM + grp * FPT);
+#pragma unroll
+                        for (int v = 0; v < FPT / 16; ++v)
+                            h4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                         if (grp == 0) args.hs_t[static_cast<size_t>(I.mb) * args.total_rows + row] = sq;
                     }
                 } else {
-                    // each lane holds its token's 64 outputs (128 bytes of bf16). Stored
+                    // each lane holds its token's HC outputs (2 HC bytes of bf16). Stored
                     // directly, one 16-byte store instruction would touch 32 rows; instead
-                    // eight rows at a time pass through this warp's 1 KB slot (16-byte
-                    // chunk v of slot row q at chunk v ^ q: conflict-free both ways) and
-                    // leave as stores of whole 128-byte row segments, four rows each.
+                    // eight rows at a time pass through this warp's slot (16-byte chunk v
+                    // of slot row q at chunk v ^ q: conflict-free both ways) and leave as
+                    // stores of whole row segments.
                     const int nout = args.num_mb * 2 * kBM;   // output features per row
                     uint4 w[HC / 8];
 #pragma unroll
@@ -686,22 +704,25 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                         w[v].z = bf16x2_bits(acc[8 * v + 4], acc[8 * v + 5]);
                         w[v].w = bf16x2_bits(acc[8 * v + 6], acc[8 * v + 7]);
                     }
-                    uint8_t *slot = s_xpose + ew * 1024;
+                    constexpr int kRowBytes = HC * 2;         // one slot row
+                    constexpr int kRowChunks = HC / 8;        // its 16-byte chunks
+                    uint8_t *slot = s_xpose + ew * 8 * kRowBytes;
                     if (quad_live) {
-                    __nv_bfloat16 *obase = args.out + static_cast<size_t>(I.mb) * 2 * kBM + grp * 64;
+                    __nv_bfloat16 *obase = args.out + static_cast<size_t>(I.mb) * 2 * kBM + grp * HC;
 #pragma unroll
                     for (int pass = 0; pass < 4; ++pass) {
                         if ((lane >> 3) == pass) {
                             const int q = lane & 7;
 #pragma unroll
-                            for (int v = 0; v < 8; ++v)
-                                *reinterpret_cast<uint4 *>(slot + q * 128 + ((v ^ q) << 4)) = w[v];
+                            for (int v = 0; v < kRowChunks; ++v)
+                                *reinterpret_cast<uint4 *>(slot + q * kRowBytes + ((v ^ q) << 4)) = w[v];
                         }
                         __syncwarp();
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const int q = (lane >> 3) + 4 * half, c = lane & 7;
-                            const uint4 v4 = *reinterpret_cast<const uint4 *>(slot + q * 128 + ((c ^ q) << 4));
+                        for (int part = 0; part < kRowChunks / 4; ++part) {
+                            const int idx = part * 32 + lane;
+                            const int q = idx / kRowChunks, c = idx % kRowChunks;
+                            const uint4 v4 = *reinterpret_cast<const uint4 *>(slot + q * kRowBytes + ((c ^ q) << 4));
                             const int tr = quad * 32 + pass * 8 + q;   // token row in the tile
                             if (tr < I.n)
                                 *reinterpret_cast<uint4 *>(obase + static_cast<size_t>(I.row0 + tr) * nout + c * 8) = v4;
@@ -931,11 +952,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     grouped_gemm_body<KIND, BN>(map_a, map_b, args);
 }
 
-// The 19-warp CTAs of the 256-row token-major kinds: each sub-partition's register
-// file (16,384 registers) holds five of the warps at 96 registers a thread, enough
-// for the epilogue's 64 accumulators and a 16-column TMEM chunk.
+// The CTAs of the 256-row token-major kinds: the register cap is what each
+// sub-partition's register file (16,384 registers) allows for its share of the
+// warps, enough for the epilogue's accumulators and a 16-column TMEM chunk.
 template <Kind KIND, int BN>
-__global__ void __maxnreg__(96)
+__global__ void __maxnreg__((KindCfg<KIND, BN>::kWideRegs))
 grouped_gemm_wide_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ ActMaps map_b,
                          const GemmArgs args) {
     grouped_gemm_body<KIND, BN>(map_a, map_b, args);
