@@ -104,16 +104,18 @@ int down_bn(const moe_cfg_t &c, int T) { return down_pair(c, T) ? 32 : 128; }
 
 int router_bn(int T) { return T <= 512 ? 32 : 128; }
 
-// Deterministic split-K of the router GEMM: the split count (1..8, at least 4 K
+// Deterministic split-K of the router GEMM: the split count (1..4, at least 4 K
 // blocks of 64 elements per split, at most two waves of items) that minimises
-// waves x K blocks per split, the smaller count on ties. A 256-token batch thus
-// runs 6 splits in one wave; a 4096-token batch 3 splits in two waves instead of
-// 96 items in one.
+// waves x K blocks per split, the smaller count on ties. Each split adds a plane
+// of partial logits that the top-k kernel reads in turn, so few splits pay: at a
+// 256-token batch 4 splits (one wave of 96 items) route 4.5 us faster than 6
+// (144 items). A 4096-token batch runs 3 splits in two waves instead of 96
+// items in one.
 int router_splits(const moe_cfg_t &c, int T) {
     const int bn = router_bn(T);
     const int items = std::max(1, ((T + bn - 1) / bn) * ((c.E + 127) / 128));
     const int num_kb = c.d / 64;
-    const int max_s = std::max(1, std::min(8, num_kb / 4));
+    const int max_s = std::max(1, std::min(4, num_kb / 4));
     const int sms = 148;   // work items per wave (the GPU's SMs less a small margin)
     int best = 1;
     long best_cost = -1;
