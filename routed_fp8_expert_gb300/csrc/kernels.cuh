@@ -19,9 +19,34 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&v)[8]) {
 }
 
 // ------------------------------------------------------------------ quantise
+// The quotients x / s of one group, correctly rounded as IEEE division rounds
+// them, by Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1),
+// 1990): with r = 1 / s correctly rounded, q0 = x r, e = x - s q0 (exact, one
+// FMA) and q = q0 + e r, each rounded to nearest, q is the correctly rounded
+// x / s when no step over- or underflows. The quotients here are at most 448 in
+// magnitude. For s >= 2^-80, e can lose bits to underflow only where the quotient
+// lies below 2^-11, under every e4m3 rounding boundary, so the codes equal those
+// of IEEE division. A zero quotient takes x's sign, as x / s does. Smaller scales
+// fall back to the division.
+template <int N>
+__device__ __forceinline__ void div_by_scale(const float (&x)[N], float s, float (&q)[N]) {
+    if (s >= 8.27180613e-25f) {   // 2^-80
+        const float r = 1.0f / s;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float q0 = x[i] * r;
+            q[i] = copysignf(fmaf(fmaf(-q0, s, x[i]), r, q0), x[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) q[i] = x[i] / s;
+    }
+}
+
 // One warp per 128-wide group: lane l holds elements 4l..4l+3.
-// s = amax / 448 (IEEE fp32 division), q = e4m3(x / s) (IEEE division, RNE,
-// saturating); amax = 0 gives s = 0 and zero codes.
+// s = amax / 448 (IEEE fp32 division), q = e4m3(x / s) (x / s correctly rounded,
+// RNE to e4m3, saturating); amax = 0 gives s = 0 and zero codes.
 template <bool kBf16In>
 __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, int cols,
                                    uint8_t *__restrict__ q, float *__restrict__ s, int s_transposed) {
@@ -32,9 +57,25 @@ __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, in
     const int64_t n_groups = rows * gpr;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    // (row, group) of the warp's group, advanced by the grid stride without a
+    // division per group (a 64-bit division is a long instruction sequence; the
+    // two here are 32-bit whenever the counts fit)
+    int64_t r, dr;
+    int g, dg;
+    if (n_groups <= 0x7fffffff) {
+        const uint32_t w0 = static_cast<uint32_t>(warp0), nw = static_cast<uint32_t>(nwarps);
+        const uint32_t ug = static_cast<uint32_t>(gpr);
+        r = w0 / ug;
+        g = static_cast<int>(w0 - static_cast<uint32_t>(r) * ug);
+        dr = nw / ug;
+        dg = static_cast<int>(nw - static_cast<uint32_t>(dr) * ug);
+    } else {
+        r = warp0 / gpr;
+        g = static_cast<int>(warp0 - r * gpr);
+        dr = nwarps / gpr;
+        dg = static_cast<int>(nwarps - dr * gpr);
+    }
     for (int64_t gi = warp0; gi < n_groups; gi += nwarps) {
-        const int64_t r = gi / gpr;
-        const int g = static_cast<int>(gi - r * gpr);
         const int64_t base = r * cols + g * 128 + lane * 4;
         float v[4];
         if constexpr (kBf16In) {
@@ -53,12 +94,20 @@ __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, in
         const float sc = amax / 448.0f;
         uint32_t packed = 0;
         if (amax != 0.f) {
-            const uint32_t lo = e4m3x2(v[0] / sc, v[1] / sc);
-            const uint32_t hi = e4m3x2(v[2] / sc, v[3] / sc);
+            float d4[4];
+            div_by_scale(v, sc, d4);
+            const uint32_t lo = e4m3x2(d4[0], d4[1]);
+            const uint32_t hi = e4m3x2(d4[2], d4[3]);
             packed = lo | (hi << 16);
         }
         *reinterpret_cast<uint32_t *>(q + base) = packed;
         if (lane == 0) s[s_transposed ? (static_cast<int64_t>(g) * rows + r) : (r * gpr + g)] = sc;
+        r += dr;
+        g += dg;
+        if (g >= gpr) {
+            g -= gpr;
+            ++r;
+        }
     }
 }
 
@@ -527,8 +576,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const __nv_bfloat16
         uint2 codes = make_uint2(0u, 0u);
         if (amax != 0.f) {
             float d8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) d8[i] = v[i] / sc;
+            div_by_scale(v, sc, d8);
             codes.x = static_cast<uint32_t>(e4m3x2(d8[0], d8[1])) | (static_cast<uint32_t>(e4m3x2(d8[2], d8[3])) << 16);
             codes.y = static_cast<uint32_t>(e4m3x2(d8[4], d8[5])) | (static_cast<uint32_t>(e4m3x2(d8[6], d8[7])) << 16);
         }

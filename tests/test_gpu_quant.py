@@ -100,13 +100,42 @@ def test_quantiser_division_every_bf16_maximum():
 
 
 def test_quantiser_division_subnormal_scales():
-    # group maxima below 448 * 2^-126 give subnormal scales, where the quantiser falls
-    # back to the plain division
+    # group maxima below 448 * 2^-126 give subnormal scales (the quantiser divides
+    # directly below scales of 2^-80)
     amax = np.ldexp(1.0 + np.arange(0, 128, 8) / 128.0, -120)
     groups = _division_sweep(amax)
     x = torch.from_numpy(groups.reshape(-1, 2048)).to(torch.bfloat16)
     q, s = _run(x)
     qo, so = O.quantize_1x128(x.float().numpy())
     assert (so < 1.17549435e-38).all()
+    np.testing.assert_array_equal(s.view(np.uint32), so.view(np.uint32))
+    np.testing.assert_array_equal(q, qo)
+
+
+def test_quantiser_division_midpoints_across_scales():
+    # scales s = (1 + m/8) 2^k from 2^-85 to 2^100, on both sides of 2^-80, below
+    # which the quantiser divides directly: each group's amax is exactly 448 s, and
+    # its entries are s times every e4m3 rounding midpoint and the fp32 neighbours
+    # of those products, so every code decision sits on or next to a boundary;
+    # bit-exact against the oracle's IEEE fp32 division
+    mids = np.array([(O.e4m3_value(c) + O.e4m3_value(c + 1)) / 2 for c in range(0x7E)])
+    groups = []
+    for k in range(-85, 101):
+        for m in (0, 3, 5):
+            s = np.float32(np.ldexp(1.0 + m / 8.0, k))
+            base = (mids * np.float64(s)).astype(np.float32)   # exact: few significant bits
+            vals = np.concatenate([base, np.nextafter(base, np.float32(0)), np.nextafter(base, np.float32(np.inf))])
+            vals = np.where(np.arange(vals.size) % 2 == 0, vals, -vals).astype(np.float32)
+            for i in range(0, vals.size, 127):
+                g = np.zeros(128, np.float32)
+                chunk = vals[i:i + 127]
+                g[:chunk.size] = chunk
+                g[127] = np.float32(448.0) * s
+                groups.append(g)
+    x = np.stack(groups)
+    pad = (-x.shape[0]) % 8
+    x = np.concatenate([x, np.zeros((pad, 128), np.float32)]).reshape(-1, 1024)
+    q, s = _run(torch.from_numpy(x))
+    qo, so = O.quantize_1x128(x)
     np.testing.assert_array_equal(s.view(np.uint32), so.view(np.uint32))
     np.testing.assert_array_equal(q, qo)
