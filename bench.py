@@ -57,11 +57,16 @@ DATA = ("synthetic, seeded: x ~ N(0,1) bf16; W_g ~ N(0,0.02) bf16; bias ~ N(0,0.
 
 # DRAM bytes (read + write) per launch of the decode gate/up kernel, from one ncu
 # capture of the same kernel on the decode-like case of a few GB (decode_e64:
-# 1.9159 GB of traffic for 1.9130 GB of algorithmic bytes). Traffic grows with
+# 1.9162 GB of traffic for 1.9130 GB of algorithmic bytes). Traffic grows with
 # the touched experts' weights, so the full launch's figure is this ratio times
 # its algorithmic bytes. Keyed by the hash of the kernel sources at capture
 # time: once the sources change, the figure no longer applies (null).
 NCU_TRAFFIC = {"ratio": 1.0016, "src": "56d706d3317c3059", "case": "decode_e64"}
+# The same for the token-major gate/up kernel in the one-tile-per-expert regime of
+# the prefill batch (prefill_e64: 96 rows per routed expert, so one 128-token tile;
+# 1.9852 GB of traffic for 1.9746 GB of algorithmic bytes), applied to workloads
+# without hot experts and with at most 128 rows per routed expert.
+NCU_TRAFFIC_WIDE = {"ratio": 1.0054, "src": "56d706d3317c3059", "case": "prefill_e64"}
 
 
 def kernel_src_hash() -> str:
@@ -384,6 +389,9 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
     traffic_val = None
     if NCU_TRAFFIC and NCU_TRAFFIC.get("src") == kernel_src_hash() and expert_bn_is_decode(shape):
         traffic_val = NCU_TRAFFIC["ratio"] * gu_bytes
+    elif (NCU_TRAFFIC_WIDE and NCU_TRAFFIC_WIDE.get("src") == kernel_src_hash() and not shape.hot_experts
+          and shape.topk * shape.T / shape.E <= 128):
+        traffic_val = NCU_TRAFFIC_WIDE["ratio"] * gu_bytes
     gu_kernel = ("grouped_gemm_kernel<GateUp, 32>" if expert_bn_is_decode(shape) else
                  "grouped_gemm_wide_kernel<GateUpWide, 128>")
     layer_weight_bytes = touched * (3 * H * d + 3 * (H // 128) * (d // 128) * 4) + E * d * 2
