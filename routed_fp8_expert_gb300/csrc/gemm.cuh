@@ -675,13 +675,33 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                         for (int g = 1; g < C::kGroups; ++g) amax = fmaxf(amax, xch[g * kBM + r]);
                         const float sq = amax / 448.0f;
                         // codes in feature order, four to a word (the first in the low byte);
-                        // an all-zero group has scale 0 and codes 0
+                        // an all-zero group has scale 0 and codes 0. The quotients h / sq
+                        // are correctly rounded by Markstein's correction step (P. Markstein,
+                        // IBM J. Res. Develop. 34(1), 1990): q0 = h r with r = 1 / sq
+                        // correctly rounded, then q0 + (h - sq q0) r, the inner term exact
+                        // by FMA. For sq >= 2^-80 an underflowing term can only touch
+                        // quotients below 2^-11, under every e4m3 rounding boundary, so the
+                        // codes are those of IEEE division; smaller scales divide.
                         uint32_t w[FPT / 4];
+                        if (sq >= 8.27180613e-25f) {   // 2^-80
+                            const float rq = 1.0f / sq;
+                            auto qd = [&](float x) -> float {
+                                const float q0 = x * rq;
+                                return copysignf(fmaf(fmaf(-q0, sq, x), rq, q0), x);
+                            };
 #pragma unroll
-                        for (int v = 0; v < FPT / 4; ++v) {
-                            const uint32_t lo = e4m3x2(acc[4 * v] / sq, acc[4 * v + 1] / sq);
-                            const uint32_t hi = e4m3x2(acc[4 * v + 2] / sq, acc[4 * v + 3] / sq);
-                            w[v] = (amax == 0.f) ? 0u : (lo | (hi << 16));
+                            for (int v = 0; v < FPT / 4; ++v) {
+                                const uint32_t lo = e4m3x2(qd(acc[4 * v]), qd(acc[4 * v + 1]));
+                                const uint32_t hi = e4m3x2(qd(acc[4 * v + 2]), qd(acc[4 * v + 3]));
+                                w[v] = lo | (hi << 16);
+                            }
+                        } else {
+#pragma unroll
+                            for (int v = 0; v < FPT / 4; ++v) {
+                                const uint32_t lo = e4m3x2(acc[4 * v] / sq, acc[4 * v + 1] / sq);
+                                const uint32_t hi = e4m3x2(acc[4 * v + 2] / sq, acc[4 * v + 3] / sq);
+                                w[v] = (amax == 0.f) ? 0u : (lo | (hi << 16));
+                            }
                         }
                         uint4 *h4 = reinterpret_cast<uint4 *>(args.hq + row * H + I.mb * kBM + grp * FPT);
 #pragma unroll
