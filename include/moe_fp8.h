@@ -81,8 +81,9 @@ size_t moe_workspace_bytes(const moe_cfg_t *cfg, int T);
  * s       [rows, cols/128] fp32, ROW-major (s_transposed = 0) or
  *         [cols/128, rows] (s_transposed = 1)
  * Per group of 128 columns: s = fp32(amax) / 448 (IEEE division);
- * q = e4m3(fp32(x) / s) (IEEE division, round to nearest even, saturate to
- * +-448); a group with amax = 0 gets s = 0 and codes 0x00. cols % 128 == 0. */
+ * q = e4m3(fp32(x) / s) (the correctly rounded fp32 quotient, as IEEE division
+ * gives it; then round to nearest even, saturate to +-448); a group with
+ * amax = 0 gets s = 0 and codes 0x00. cols % 128 == 0. */
 int moe_quant_fp8_1x128(const void *in, int in_is_bf16, int64_t rows, int cols,
                         uint8_t *q, float *s, int s_transposed, void *stream);
 
