@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const __nv_bfloat16
 // per thread, for batches too small to fill the GPU with CTAs); it needs rows of
 // at most 256 threads (d <= 8192), for the register room (up to 128 a thread).
 // Without it the launch bound is 1024 threads and 64 registers, for the occupancy
-// that large batches want.
+// that large batches want, and the rows are loaded four slots at a time.
 template <bool kBatch>
 __global__ void __launch_bounds__(kBatch ? 256 : 1024, kBatch ? 2 : 1) combine_residual_rmsnorm_kernel(
     const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w, const int32_t *__restrict__ inv_pos, int T,
@@ -663,13 +663,26 @@ __global__ void __launch_bounds__(kBatch ? 256 : 1024, kBatch ? 2 : 1) combine_r
                 }
             }
         } else {
-            for (int j = 0; j < k; ++j) {
-                if (s_pos[j] < 0) continue;
-                float e[8];
-                unpack_bf16x8(reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v], e);
-                const float wj = s_w[j];
+            // four slots at a time within the 64-register budget of this variant
+            for (int j0 = 0; j0 < k; j0 += 4) {
+                uint4 raw[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, e[i], acc[i]);
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = j0 + jj;
+                    raw[jj] = make_uint4(0u, 0u, 0u, 0u);
+                    if (j < k && s_pos[j] >= 0)
+                        raw[jj] = reinterpret_cast<const uint4 *>(o + static_cast<size_t>(s_pos[j]) * d)[v];
+                }
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = j0 + jj;
+                    if (j >= k || s_pos[j] < 0) continue;
+                    float e[8];
+                    unpack_bf16x8(raw[jj], e);
+                    const float wj = s_w[j];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, e[i], acc[i]);
+                }
             }
         }
         float yb[8], res[8];
