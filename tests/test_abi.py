@@ -109,3 +109,35 @@ def test_negative_and_zero_tokens(lib):
     assert lib.moe_last_launch_count() == 0
     assert lib.dense_swiglu_fp8(None, None, None, None, None, 1024, 256, 0, None, None, 0, None) == _lib.MOE_OK
     assert lib.moe_quant_fp8_1x128(None, 1, 0, 128, None, None, 0, None) == _lib.MOE_OK
+
+
+def test_plain_c_caller(lib, tmp_path):
+    # the header compiles as C99 and a C program links against the library and calls
+    # it: the host-side calls (sizes, argument checks) need no GPU
+    src = tmp_path / "caller.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "moe_fp8.h"
+int main(void) {
+    moe_cfg_t cfg = {7168, 384, 8, 2048, 1, 2.827f};
+    printf("%lld %zu\n", (long long)moe_permuted_rows(&cfg, 256), moe_workspace_bytes(&cfg, 256));
+    moe_cfg_t bad = {100, 384, 8, 2048, 1, 2.827f};   /* d not a multiple of 128 */
+    printf("%d\n", moe_combine(NULL, NULL, NULL, &bad, 4, NULL, NULL));
+    printf("%s\n", moe_last_error_string() ? "msg" : "none");
+    return 0;
+}
+''')
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    import subprocess
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                        "-L", libdir, "-lmoe_fp8", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    lines = out.stdout.split()
+    cfg = _lib.MoeCfg(7168, 384, 8, 2048, 1, 2.827)
+    assert int(lines[0]) == moe.permuted_rows(cfg, 256)
+    assert int(lines[1]) == moe.workspace_bytes(cfg, 256)
+    assert int(lines[2]) in (_lib.MOE_ERR_ARG, _lib.MOE_ERR_UNSUPPORTED)
+    assert lines[3] == "msg"
