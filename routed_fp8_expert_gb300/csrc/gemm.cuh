@@ -217,7 +217,12 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and division intrinsics
+// (__expf, __fdividef: a few ulp of fp32, far inside the h quantiser's rounding
+// step); IEEE division here made the per-item epilogue tail a tenth of the
+// wide gate/up kernel's time, with the tensor pipe idle behind it. For g below
+// about -87, e^-g overflows and the quotient is 0, silu's limit.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // acc[i] += s * p[i], i < 16, as eight two-lane packed FMAs: each lane is an
 // ordinary fma.rn, so the sums equal fmaf's bit for bit with half the issue slots

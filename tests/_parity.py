@@ -1,7 +1,8 @@
 """Shared checks of the GPU parity tests.
 
 Tolerances (layer outputs, fp64 oracle as reference): max |y - ref| <= 2e-2 RMS(ref)
-and mean |y - ref| / mean |ref| <= 5e-3. Routing: expert ids identical except for
+(plus the bf16 storage rounding of ref, element by element) and
+mean |y - ref| / mean |ref| <= 5e-3. Routing: expert ids identical except for
 tokens whose k-th / (k+1)-th biased-score gap is below 1e-5, where the GPU's set
 must be a valid top-k within 1e-5 of the oracle's k-th score.
 """
@@ -13,14 +14,33 @@ MEAN_REL = 5e-3
 TIE_GAP = 1e-5
 
 
-def assert_close_layer(y, ref, what=""):
+def bf16_half_ulp(ref):
+    """Half a bf16 ulp at |ref|: the largest error of rounding ref to bf16 (8
+    significant bits), 2^(floor(log2|ref|) - 8)."""
+    a = np.abs(np.asarray(ref, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 8), 0.0)
+
+
+def assert_close_layer(y, ref, what="", bf16_out=True):
+    """max|y - ref| <= 2e-2 RMS(ref) and mean|y - ref| / mean|ref| <= 5e-3.
+
+    The outputs checked here (the layer's y, the experts' o, the dense FFN's y) are
+    bf16 tensors, while ref is the oracle's fp64 value before rounding: element by
+    element the bound on the max error adds the half-ulp that storing ref in bf16
+    may cost (2^-8 |ref| at most, 1-2% of RMS at a 4-5 sigma output), so that the
+    computation, not the storage format, is what the tolerance judges."""
     y = y.float().cpu().numpy() if isinstance(y, torch.Tensor) else np.asarray(y, np.float64)
     ref = np.asarray(ref, np.float64)
     assert np.isfinite(y).all(), f"{what}: non-finite output"
     err = np.abs(y - ref)
     rms = np.sqrt((ref ** 2).mean())
     mean_rel = err.mean() / np.abs(ref).mean()
-    assert err.max() <= MAX_REL_RMS * rms, f"{what}: max|err| {err.max():.3e} > {MAX_REL_RMS} * RMS {rms:.3e}"
+    allow = MAX_REL_RMS * rms + (bf16_half_ulp(ref) if bf16_out else 0.0)
+    excess = err - allow
+    i = np.unravel_index(np.argmax(excess), err.shape)
+    assert excess[i] <= 0, (f"{what}: |err| {err[i]:.3e} at {i} > {MAX_REL_RMS} * RMS {rms:.3e}"
+                            f"{' + bf16 half-ulp of ref' if bf16_out else ''} ({allow[i] if np.ndim(allow) else allow:.3e})")
     assert mean_rel <= MEAN_REL, f"{what}: mean relative error {mean_rel:.3e} > {MEAN_REL}"
     return err.max() / rms, mean_rel
 

@@ -12,12 +12,18 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def _run(shape, seed, n_check=None):
+def _run(shape, seed, n_check=None, hot=()):
     inp = S.gen_moe_inputs(shape, seed=seed, device="cpu")
     cfg = moe.cfg_of(shape)
     T, k = shape.T, shape.topk
     rng = np.random.default_rng(seed)
-    idx = np.stack([rng.choice(shape.E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    if hot:
+        # each token takes the hot experts with probability 0.9 each, then cold ones
+        p = np.full(shape.E, 0.1 / (shape.E - len(hot)))
+        p[list(hot)] = 0.9 / len(hot)
+        idx = np.stack([rng.choice(shape.E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    else:
+        idx = np.stack([rng.choice(shape.E, k, replace=False) for _ in range(T)]).astype(np.int32)
     ex = inp.experts.to(DEV)
     xq, sx = moe.quant_fp8_1x128(inp.x.to(DEV))
     offsets, sorted_tok, inv_pos, xq_perm, sx_perm = moe.permute(torch.from_numpy(idx).to(DEV), xq, sx, cfg)
@@ -57,9 +63,24 @@ def test_experts_with_several_token_tiles():
 
 
 def test_experts_beyond_128_rows_span_several_token_tiles():
-    # 150 rows per routed expert and 600 shared rows: two or more 128-token tiles per expert
+    # 150 rows per routed expert and 600 shared rows: two or more 128-token tiles per
+    # expert, the last one ragged; every row is compared
     shape = S.MoEShape("wide_tiles", T=600, d=512, E=32, topk=8, H=256)
-    assert _run(shape, seed=3, n_check=40) > 0
+    assert _run(shape, seed=3) == 9 * 600
+
+
+def test_several_tiles_with_odd_down_blocks():
+    # 150 rows per routed expert with d = 384: several token tiles per expert, and the
+    # down projection (three 128-row output blocks) on the one-block kernel
+    shape = S.MoEShape("pair_odd_d", T=600, d=384, E=32, topk=8, H=384)
+    assert _run(shape, seed=6) == 9 * 600
+
+
+def test_skewed_segments_many_tiles_and_few_rows():
+    # skewed routing at toy size: four hot experts with about 590 rows each (five
+    # 128-token tiles, the last ragged) and cold experts of a few dozen rows
+    shape = S.MoEShape("pair_ragged", T=700, d=256, E=16, topk=4, H=256)
+    assert _run(shape, seed=7, hot=(0, 5, 9, 12)) == 5 * 700
 
 
 def test_decode_down_with_odd_block_count():
