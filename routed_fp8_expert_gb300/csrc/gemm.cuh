@@ -127,7 +127,9 @@ struct GemmArgs {
     int total_rows;           // rows of the activation buffer
     int single_rows;          // >= 0: one group of that many rows (row_start / tile_prefix unused)
     const int *row_start;     // [G+1] first activation row of each group's segment
-    const int *tile_prefix;   // [G+1] prefix sum of ceil(rows_g / BN)
+    const int *tile_prefix;   // [2][G+1] prefix sums of ceil(rows_g / BN): all groups, then those
+                              // of two or more tiles only
+    int interleave;           // merge the items of multi-tile groups with those of one-tile groups
     const float *act_scale_t; // [num_kb][total_rows]  (FP8 kinds)
     const float *w_scale;     // GateUp: [G][2][num_mb][num_kb]; Down: [G][num_mb][num_kb]
     int a_rows_per_group;     // weight rows of one group in the A tensor map (GateUp: 2*H, Down: d_out)
@@ -148,9 +150,18 @@ struct Item {
 
 // Items of a group are ordered (weight block, token tile) with the token tile
 // fastest, so the tiles that share a weight block are adjacent.
+//
+// Interleaved order (a.interleave): the items of groups with two or more token
+// tiles (weight blocks re-read from L2 by every tile: tensor-bound) and those of
+// one-tile groups (weights streamed from HBM once) form two streams, each in the
+// order above, merged evenly: item i is the m-th of the multi-tile stream when
+// floor((i+1) NM / N) > floor(i NM / N) = m (NM of N items multi-tile), else
+// the (i - m)-th single-tile item. Under skewed routing the HBM streaming of the
+// cold experts then overlaps the hot experts' MMAs instead of alternating with them.
+// s_tpm[g] is the multi-tile prefix; the single-tile prefix is s_tp[g] - s_tpm[g].
 template <int BN>
 __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int *s_tp,
-                                            const int *s_rs, Item &o) {
+                                            const int *s_rs, const int *s_tpm, Item &o) {
     const int nblk = a.num_mb;   // weight blocks per group
     int mbx;
     if (a.single_rows >= 0) {
@@ -167,22 +178,34 @@ __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int
         o.ntiles = nt_total;
     } else {
         o.ks = 0;
-        const int key = it / nblk;
-        int lo = 0, hi = a.G;  // find the last g with tile_prefix[g] <= key
+        int idx = it;          // index inside the item's stream
+        int stream = 0;        // 0: all groups (plain order), 1: multi-tile, 2: one-tile
+        if (a.interleave) {
+            const long long n_all = static_cast<long long>(nblk) * s_tp[a.G];
+            const long long n_multi = static_cast<long long>(nblk) * s_tpm[a.G];
+            const long long m0 = static_cast<long long>(it) * n_multi / n_all;
+            const long long m1 = static_cast<long long>(it + 1) * n_multi / n_all;
+            if (m1 > m0) { idx = static_cast<int>(m0); stream = 1; }
+            else { idx = it - static_cast<int>(m0); stream = 2; }
+        }
+        // the stream's tile prefix at group g
+        auto prefix = [&](int g) -> int { return stream == 0 ? s_tp[g] : stream == 1 ? s_tpm[g] : s_tp[g] - s_tpm[g]; };
+        const int key = idx / nblk;
+        int lo = 0, hi = a.G;  // find the last g with prefix(g) <= key (a group of the stream)
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (s_tp[mid] <= key) lo = mid; else hi = mid;
+            if (prefix(mid) <= key) lo = mid; else hi = mid;
         }
         const int g = lo;
-        const int nt_g = s_tp[g + 1] - s_tp[g];
+        const int nt_g = prefix(g + 1) - prefix(g);
         if (nt_g <= 0) return false;
-        const int li = it - nblk * s_tp[g];
+        const int li = idx - nblk * prefix(g);
         o.g = g;
         mbx = li / nt_g;
         const int nt = li - mbx * nt_g;
         o.row0 = s_rs[g] + nt * BN;
         o.n = min(BN, s_rs[g + 1] - o.row0);
-        o.ntiles = nt_g;
+        o.ntiles = s_tp[g + 1] - s_tp[g];
     }
     o.mb = mbx;
     return o.n > 0 && o.mb < a.num_mb;
@@ -246,8 +269,9 @@ template <Kind KIND, int BN> struct SmemLayout {
     static constexpr size_t kItems = kMisc + 16;                                // [kItemQ] int
     static constexpr size_t kTp = kItems + kItemQ * 4;
     static constexpr size_t kRs = kTp + kMaxGroups * 4;
+    static constexpr size_t kTpm = kRs + kMaxGroups * 4;                       // [kMaxGroups] multi-tile prefix
     static constexpr int kScaleStride = BN + 4;                                // floats per stage: BN act + 2 weight
-    static constexpr size_t kScale = kRs + kMaxGroups * 4;                     // [kScaleSlots][kScaleStride]
+    static constexpr size_t kScale = kTpm + kMaxGroups * 4;                    // [kScaleSlots][kScaleStride]
     static constexpr size_t kCs = kScale + C::kScaleSlots * kScaleStride * 4;  // [warps][2][kATiles][HC], swap-AB
     static constexpr size_t kAmax = kCs + (C::kTM ? 0 : C::kEpiWarps * 2 * C::kATiles * C::kHalfCols * 4);
     // the h amax exchange: GateUp [groups][2][4][HC]; GateUpWide [2][4 groups][128 rows]
@@ -299,6 +323,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     volatile int *s_items = reinterpret_cast<volatile int *>(smem + L::kItems);
     int *s_tp = reinterpret_cast<int *>(smem + L::kTp);
     int *s_rs = reinterpret_cast<int *>(smem + L::kRs);
+    int *s_tpm = reinterpret_cast<int *>(smem + L::kTpm);
     float *s_scale = reinterpret_cast<float *>(smem + L::kScale);  // scale slots
     float *s_cs = reinterpret_cast<float *>(smem + L::kCs);        // per-warp combined scales
     float *s_amax = reinterpret_cast<float *>(smem + L::kAmax);
@@ -340,6 +365,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         for (int i = threadIdx.x; i <= args.G; i += blockDim.x) {
             s_tp[i] = args.tile_prefix[i];
             s_rs[i] = args.row_start[i];
+            if (args.interleave) s_tpm[i] = args.tile_prefix[args.G + 1 + i];
         }
     }
     tc_fence_before();
@@ -418,7 +444,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             if (!got || it >= n_items) break;
             if (++q == kItemQ) { q = 0; qphase ^= 1; }
             Item I;
-            if (!decode_item<BN>(it, args, s_tp, s_rs, I)) {
+            if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) {
                 if (lane == 0) record_error(args.err, ERR_BAD_TILE);
                 continue;
             }
@@ -488,7 +514,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 const int it = take_item(q, qphase);
                 if (it < 0 || it >= n_items) break;
                 Item I;
-                if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
+                if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) continue;
                 int kb0, kb1;
                 kb_range(args, I, kb0, kb1);
                 // swap-AB: M = 128 weight rows, N = the tile's tokens rounded up to 16;
@@ -554,7 +580,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             it = __shfl_sync(0xffffffffu, it, 0);
             if (it < 0 || it >= n_items) break;
             Item I;
-            if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
+            if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) continue;
             const float *ws0, *ws1;
             weight_scale_rows(I, ws0, ws1);
             for (int kb = 0; kb < args.num_kb; ++kb) {
@@ -589,7 +615,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             it = __shfl_sync(0xffffffffu, it, 0);
             if (it < 0 || it >= n_items) break;
             Item I;
-            if (!decode_item<BN>(it, args, s_tp, s_rs, I)) continue;
+            if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) continue;
             const int n_my = max(0, min(HC, I.n - col_base));
             if constexpr (C::kWide) {
                 // token-major, 256 weight rows: thread = token row r; its HC accumulators are

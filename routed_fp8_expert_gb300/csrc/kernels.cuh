@@ -313,11 +313,12 @@ __device__ void block_exclusive_scan(const int32_t *in, int n, int32_t *out, int
 
 // Segment table of the grouped GEMMs from the routed offsets: groups 0..E-1
 // are the routed experts' segments, groups E..E+S-1 the shared experts' T rows.
-//   row_start[g]        first activation row of group g; row_start[E+S] = (k+S)*T
-//   tile_prefix_a/b[g]  prefix sums of ceil(rows_g / tile_a) and ceil(rows_g / tile_b)
-// (the gate/up and the down GEMM may use different token-tile widths), and the
-// two GEMMs' dynamic scheduler counters are reset to zero.
-// Called by a whole block of 1024 threads (E + S <= 1028).
+//   row_start[g]              first activation row of group g; row_start[E+S] = (k+S)*T
+//   tile_prefix_a/b[g]        prefix sums of ceil(rows_g / tile_a) and ceil(rows_g / tile_b)
+//   tile_prefix_a/b[G+1+g]    the same over the groups of two or more tiles only
+// (the gate/up and the down GEMM may use different token-tile widths; each array
+// holds 2 (G+1) entries), and the two GEMMs' dynamic scheduler counters are reset
+// to zero. Called by a whole block of 1024 threads (E + S <= 1028).
 __device__ void schedule_block(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
                                int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b,
                                int32_t *counters) {
@@ -333,6 +334,9 @@ __device__ void schedule_block(const int32_t *offsets, int E, int S, int T, int 
     }
     __syncthreads();
     block_exclusive_scan<2>(s_rows, G, tile_prefix_a, tile_prefix_a + G);
+    for (int g = threadIdx.x; g < G; g += blockDim.x) s_rows[g] = (s_rows[g] >= 2) ? s_rows[g] : 0;
+    __syncthreads();
+    block_exclusive_scan<2>(s_rows, G, tile_prefix_a + G + 1, tile_prefix_a + 2 * G + 1);
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
         const int a = (g < E) ? offsets[g] : kT + (g - E) * T;
         const int b = (g < E) ? offsets[g + 1] : kT + (g - E + 1) * T;
@@ -340,6 +344,9 @@ __device__ void schedule_block(const int32_t *offsets, int E, int S, int T, int 
     }
     __syncthreads();
     block_exclusive_scan<2>(s_rows, G, tile_prefix_b, tile_prefix_b + G);
+    for (int g = threadIdx.x; g < G; g += blockDim.x) s_rows[g] = (s_rows[g] >= 2) ? s_rows[g] : 0;
+    __syncthreads();
+    block_exclusive_scan<2>(s_rows, G, tile_prefix_b + G + 1, tile_prefix_b + 2 * G + 1);
 }
 
 // offsets[0..E] from counts[0..E-1], then the GEMM schedules. Single block of 1024 threads.

@@ -32,8 +32,8 @@ constexpr size_t kCntOff = kRankOff + align64(kMaxAssignments);
 constexpr size_t kCountsOff = kCntOff + align64(static_cast<size_t>(kMaxExperts) * kMaxChunks);
 constexpr size_t kRowStartOff = kCountsOff + align64(kMaxExperts);
 constexpr size_t kTileAOff = kRowStartOff + align64(kMaxExperts + kMaxShared + 1);
-constexpr size_t kTileBOff = kTileAOff + align64(kMaxExperts + kMaxShared + 1);
-constexpr size_t kCountersOff = kTileBOff + align64(kMaxExperts + kMaxShared + 1);
+constexpr size_t kTileBOff = kTileAOff + align64(2 * (kMaxExperts + kMaxShared + 1));
+constexpr size_t kCountersOff = kTileBOff + align64(2 * (kMaxExperts + kMaxShared + 1));
 constexpr size_t kScratchWords = kCountersOff + 64;   // about 1.3 MB
 
 }  // namespace
