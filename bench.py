@@ -1,21 +1,25 @@
 #!/usr/bin/env python3
 """Throughput of the routed FP8 MoE FFN layer forward (Kimi K2 shapes) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|skewed40|dense]
-                    [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--workload all|decode|prefill|skewed|skewed40|dense] [--impl ours|reference]
 
 One step = one forward of the whole layer over one batch of T tokens already
 resident in HBM: router GEMM + top-k, x quantisation, permutation, grouped
-gate/up and down FP8 GEMMs, combine. The default workload is the decode batch
-(T=256, d=7168, 384 routed experts top-8 + 1 shared, expert hidden 2048).
-Under torchrun each rank runs an independent replica on its own batch
-(weak scaling; no collective on the data path).
+gate/up and down FP8 GEMMs, combine. The headline workload is the decode batch
+(T=256, d=7168, 384 routed experts top-8 + 1 shared, expert hidden 2048). By
+default (--workload all) the same run then measures the prefill batch (T=4096),
+the two skewed batches (T=16384) and the dense FFN of the first block
+(T=8192, H=18432) and reports each under "workloads". Under torchrun each rank
+runs an independent replica on its own batch (weak scaling; no collective on
+the data path).
 
-Prints one JSON line (rank 0). Besides the throughput it reports the
-roofline of the dominant kernel (the gate/up grouped GEMM, timed with CUDA
-events inside the timed region), the end-to-end throughput through
-moe_layer_forward with pinned host buffers, the CPU oracle timed on a token
-sample, and the SM clocks sampled during the timed region.
+Prints one JSON line (rank 0). Besides the throughput each workload reports the
+roofline of its dominant kernel (the gate/up grouped GEMM, timed with CUDA
+events inside the timed region; the whole FFN for the dense workload) against
+the measured and the nominal peaks, the end-to-end throughput through the
+one-call API with pinned host buffers, the CPU oracle timed on a token sample,
+and the SM clocks sampled during its timed region.
 """
 from __future__ import annotations
 
@@ -284,14 +288,56 @@ def workload_config(shape) -> dict:
     return cfg
 
 
+# ------------------------------------------------------------------ rooflines
+
+NOMINAL_HBM_GBS = 8000.0       # GB300 HBM3e, vendor figure (about 8 TB/s)
+NOMINAL_FP8_TFLOPS = 4500.0    # GB300 dense FP8 tensor, vendor figure
+
+
+def roofline(kernel, alg_bytes, alg_flops, ms, peaks, traffic=None, impl_bytes=None):
+    """The launch's binding roofline: whichever of its algorithmic HBM bytes and its
+    FP8 FLOPs takes longer at the measured peak. Fractions against the measured
+    peak (frac; for FP8 2 x the measured bf16 burst, and frac_sustained against 2 x
+    the sustained figure) and against the vendor's nominal figure (frac_nominal)."""
+    fp8_peak = 2 * peaks["bf16_tflops"]
+    tensor = alg_flops / (fp8_peak * 1e12) > alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    out = {"kernel": kernel, "alg_bytes_per_launch": alg_bytes, "alg_flops_per_launch": alg_flops, "launch_ms": ms}
+    if impl_bytes is not None:
+        out["impl_bytes_per_launch"] = impl_bytes
+    if tensor:
+        a = alg_flops / (ms * 1e-3) / 1e12
+        out.update({"bound": "tensor", "achieved": a, "peak": fp8_peak, "unit": "TFLOP/s", "frac": a / fp8_peak,
+                    "frac_sustained": a / (2 * peaks["bf16_tflops_sustained"]), "frac_nominal": a / NOMINAL_FP8_TFLOPS,
+                    "traffic": traffic,
+                    "peak_source": peaks["source"] + " bf16 burst x 2 (nominal fp8/bf16 ratio); frac_nominal against "
+                                   f"{NOMINAL_FP8_TFLOPS:.0f} TFLOP/s"})
+    else:
+        a = alg_bytes / (ms * 1e-3) / 1e9
+        out.update({"bound": "hbm", "achieved": a, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": a / peaks["hbm_gbs"], "frac_nominal": a / NOMINAL_HBM_GBS, "traffic": traffic,
+                    "peak_source": peaks["source"] + " hbm_gbs copy bandwidth; frac_nominal against "
+                                   f"{NOMINAL_HBM_GBS:.0f} GB/s"})
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 
-def run_moe(args, shape, rank, local, world, dev, peaks):
+def cpu_baseline_moe(shape, x, wg, b, ex, idx, n_tokens, seed):
+    """The fp64 oracle on a bounded token sample of the workload (host cores)."""
+    toks = sample_tokens(shape.T, n_tokens, seed=seed)
+    host = host_experts_from_device(ex, experts_for(idx.cpu().numpy()[toks], shape), shape)
+    tps, dt = oracle_tokens_per_s(x.cpu()[toks], wg.cpu(), b.cpu(), host, shape)
+    return {"value": tps, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+            "sample": f"{len(toks)} of {shape.T} tokens through the fp64 oracle ({dt:.1f} s)"}
+
+
+def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
     import routed_fp8_expert_gb300 as moe
     cfg = moe.cfg_of(shape)
     T, d, H, k, E, Sh = shape.T, shape.d, shape.H, shape.topk, shape.E, shape.n_shared
     R = (k + Sh) * T
-    ex = S.gen_experts(E + Sh, d, H, seed=args.seed, device=dev)
+    if ex is None:
+        ex = S.gen_experts(E + Sh, d, H, seed=args.seed, device=dev)
     x = S.gen_x(T, d, seed=args.seed + rank, device=dev)
     wg, b = S.gen_router(shape, seed=args.seed, device=dev)
     ws = moe.workspace(cfg, T, dev)
@@ -376,22 +422,19 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
     # routing statistics of the last step
     counts = torch.diff(offsets).cpu().numpy()
     touched = int((counts > 0).sum()) + Sh
-    # algorithmic bytes of one gate/up launch: touched experts' gate+up weights and
-    # scales, the permuted activation rows and scales read, h and its scales written
-    gu_bytes = (touched * (2 * H * d + 2 * (H // 128) * (d // 128) * 4)
-                + R * d + R * (d // 128) * 4 + R * H + R * (H // 128) * 4)
+    # one gate/up launch: algorithmic bytes are the touched experts' gate+up weights
+    # and scales and the step's activation codes read once; the permuted copies read
+    # and the h codes written are the implementation's own traffic, kept apart
+    gu_bytes = touched * (2 * H * d + 2 * (H // 128) * (d // 128) * 4) + T * (d + (d // 128) * 4)
+    gu_impl = R * d + R * (d // 128) * 4 + R * H + R * (H // 128) * 4
     gu_ms = per["gateup"]
     gu_flops = 4 * R * H * d
-    fp8_peak = 2 * peaks["bf16_tflops"]
-    # the launch's bound: whichever of its HBM bytes and its FP8 FLOPs takes longer at peak
-    tensor_bound = gu_flops / (fp8_peak * 1e12) > gu_bytes / (peaks["hbm_gbs"] * 1e9)
-    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
     traffic_val = None
     if NCU_TRAFFIC and NCU_TRAFFIC.get("src") == kernel_src_hash() and expert_bn_is_decode(shape):
-        traffic_val = NCU_TRAFFIC["ratio"] * gu_bytes
+        traffic_val = NCU_TRAFFIC["ratio"] * (gu_bytes + gu_impl)
     elif (NCU_TRAFFIC_WIDE and NCU_TRAFFIC_WIDE.get("src") == kernel_src_hash() and not shape.hot_experts
           and shape.topk * shape.T / shape.E <= 128):
-        traffic_val = NCU_TRAFFIC_WIDE["ratio"] * gu_bytes
+        traffic_val = NCU_TRAFFIC_WIDE["ratio"] * (gu_bytes + gu_impl)
     gu_kernel = ("grouped_gemm_kernel<GateUp, 32>" if expert_bn_is_decode(shape) else
                  "grouped_gemm_wide_kernel<GateUpWide, 128>")
     layer_weight_bytes = touched * (3 * H * d + 3 * (H // 128) * (d // 128) * 4) + E * d * 2
@@ -427,25 +470,18 @@ def run_moe(args, shape, rank, local, world, dev, peaks):
     e2e_value = tokens_total / (e2e_ms * 1e-3)
     same = torch.equal(yd, y)
     pieces = time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks)
+    step_bytes = layer_weight_bytes + 2 * T * d * 2
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3", "data": DATA, "config": workload_config(shape),
-        "roofline": ({"bound": "tensor", "kernel": gu_kernel, "achieved": gu_flops / (gu_ms * 1e-3) / 1e12,
-                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / (gu_ms * 1e-3) / 1e12 / fp8_peak,
-                      "traffic": None, "alg_flops_per_launch": gu_flops, "alg_bytes_per_launch": gu_bytes,
-                      "launch_ms": gu_ms,
-                      "peak_source": peaks["source"] + " bf16 burst x 2 (nominal fp8/bf16 ratio)"}
-                     if tensor_bound else
-                     {"bound": "hbm", "kernel": gu_kernel, "achieved": achieved,
-                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                      "traffic": traffic_val, "alg_bytes_per_launch": gu_bytes, "alg_flops_per_launch": gu_flops,
-                      "launch_ms": gu_ms,
-                      "peak_source": peaks["source"] + " (MEASURED_PEAKS hbm_gbs copy bandwidth)"}),
-        "layer": {"alg_weight_bytes": layer_weight_bytes, "hbm_frac_whole_step":
-                  (layer_weight_bytes + 2 * T * d * 2) / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "roofline": roofline(gu_kernel, gu_bytes, gu_flops, gu_ms, peaks, traffic_val, gu_impl),
+        "layer": {"alg_weight_bytes": layer_weight_bytes, "alg_bytes_whole_step": step_bytes,
+                  "hbm_frac_whole_step": step_bytes / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "hbm_frac_nominal_whole_step": step_bytes / (ms_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
                   "tflops": flops / (ms_step * 1e-3) / 1e12, "fp8_peak_tflops": 2 * peaks["bf16_tflops"],
+                  "fp8_frac_whole_step": flops / (ms_step * 1e-3) / 1e12 / (2 * peaks["bf16_tflops"]),
                   "touched_experts": touched, "max_rows_per_expert": int(counts.max()),
                   **({"hot_share": float(counts[list(shape.hot_experts)].sum() / counts[:E].sum())}
                      if shape.hot_experts else {}),
@@ -501,7 +537,7 @@ def time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks, n=50):
     return out
 
 
-def run_dense(args, shape, rank, world, dev, peaks):
+def run_dense(args, shape, rank, world, dev, peaks, want_cpu=False):
     import routed_fp8_expert_gb300 as moe
     T, d, H = shape.T, shape.d, shape.H
     inp = S.gen_dense_inputs(shape, seed=args.seed, device=dev)
@@ -521,7 +557,6 @@ def run_dense(args, shape, rank, world, dev, peaks):
     barrier(world)
     clocks.start()
     launches = 0
-    total = 0.0
     for i in range(args.steps):
         flush.zero_()   # evict the 0.4 GB of weights from L2 between steps
         ev[i][0].record()
@@ -530,23 +565,66 @@ def run_dense(args, shape, rank, world, dev, peaks):
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
+    moe.check_device_error(dev)
     total = sum(a.elapsed_time(b_) for a, b_ in ev)
     ms_total = max_over_ranks(total, world, dev)
     flops = 6.0 * T * d * H
     ms = ms_total / args.steps
-    tf = flops / (ms * 1e-3) / 1e12
-    peak = 2 * peaks["bf16_tflops"]
     tokens_total = sum_over_ranks(T * args.steps, world, dev)
+    w_bytes = 3 * H * d + 3 * (H // 128) * (d // 128) * 4
+
+    # end to end through dense_swiglu_fp8 with pinned host buffers: x in, y out,
+    # each step (no L2 flush needed: the copies pass 0.23 GB through it)
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(inp.x)
+
+    def e2e_step():
+        xd.copy_(x_host, non_blocking=True)
+        moe.dense_swiglu_fp8(xd, inp.w13, inp.w13_s, inp.w2, inp.w2_s, ws=ws, y=y)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     line = {
         "metric": METRIC, "value": tokens_total / (ms_total * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": DATA,
         "config": dict(workload_config(shape), l2="L2 flushed between steps (256 MB write)"),
-        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
-                     "traffic": None, "peak_source": peaks["source"] + " bf16 burst x 2 (nominal fp8/bf16 ratio)"},
-        "e2e": None, "gpu_launches": launches, "clocks": clk,
+        "roofline": roofline("dense_swiglu_fp8 (quantise + GateUpWide + DownWide)", w_bytes + 2 * T * d * 2, flops,
+                             ms, peaks),
+        "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * d * 2,
+                "d2h_bytes_per_step": T * d * 2, "api": "dense_swiglu_fp8"},
+        "gpu_launches": launches, "clocks": clk,
     }
+    if want_cpu:
+        toks = sample_tokens(T, args.cpu_tokens, seed=args.seed)
+        from oracle import moe_oracle as O
+        w13, w13_s, w2, w2_s = inp.w13.cpu(), inp.w13_s.cpu(), inp.w2.cpu(), inp.w2_s.cpu()
+        xs = inp.x.cpu()[toks]
+        t0 = time.perf_counter()
+        O.dense_swiglu(xs, w13, w13_s, w2, w2_s)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": len(toks) / dt, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+                                "sample": f"{len(toks)} of {T} tokens through the fp64 oracle ({dt:.1f} s)"}
     return line
+
+
+# the workloads a default run measures besides the decode headline
+EXTRA_WORKLOADS = ("prefill", "skewed", "skewed40", "dense")
+SUMMARY_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "layer", "e2e",
+                "cpu_baseline", "gpu_launches", "clocks", "block_pieces")
 
 
 def main():
@@ -554,7 +632,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--workload", choices=["all"] + sorted(WORKLOADS), default="all",
+                    help="all (default): the decode line plus every other workload under 'workloads'")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-tokens", type=int, default=4, help="tokens in the oracle's timed sample")
@@ -563,7 +642,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
-    shape = WORKLOADS[args.workload]
+    shape = WORKLOADS["decode" if args.workload == "all" else args.workload]
     rank, local, world = dist_env()
 
     if args.impl == "reference":
@@ -578,22 +657,32 @@ def main():
     torch.cuda.set_device(dev)
     init_group(world, "nccl")
     peaks = measured_peaks()
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     if isinstance(shape, S.DenseShape):
-        line = run_dense(args, shape, rank, world, dev, peaks)
-        extra = None
+        line = run_dense(args, shape, rank, world, dev, peaks, want_cpu=want_cpu)
     else:
         line, extra = run_moe(args, shape, rank, local, world, dev, peaks)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        if isinstance(shape, S.DenseShape):
-            line["cpu_baseline"] = None
-        else:
+        if want_cpu:
             x, wg, b, ex, idx = extra
-            toks = sample_tokens(shape.T, args.cpu_tokens, seed=args.seed)
-            host = host_experts_from_device(ex, experts_for(idx.cpu().numpy()[toks], shape), shape)
-            tps, dt = oracle_tokens_per_s(x.cpu()[toks], wg.cpu(), b.cpu(), host, shape)
-            line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
-                                    "sample": f"{len(toks)} of {shape.T} tokens through the fp64 oracle "
-                                              f"({dt:.1f} s)"}
+            line["cpu_baseline"] = cpu_baseline_moe(shape, x, wg, b, ex, idx, args.cpu_tokens, args.seed)
+        if args.workload == "all":
+            # every other workload, each with its own roofline, clocks, end-to-end figure
+            # and oracle sample; the MoE batches reuse the step's 16.96 GB of weights
+            ex = extra[3]
+            wl = {}
+            for name in EXTRA_WORKLOADS:
+                wshape = WORKLOADS[name]
+                if isinstance(wshape, S.DenseShape):
+                    wline = run_dense(args, wshape, rank, world, dev, peaks, want_cpu=want_cpu)
+                else:
+                    wline, wextra = run_moe(args, wshape, rank, local, world, dev, peaks, ex=ex)
+                    if want_cpu:
+                        x, wg, b, _, idx = wextra
+                        wline["cpu_baseline"] = cpu_baseline_moe(wshape, x, wg, b, ex, idx, max(1, args.cpu_tokens // 2),
+                                                                 args.seed)
+                    del wextra
+                wl[name] = {key: wline[key] for key in SUMMARY_KEYS if key in wline}
+            line["workloads"] = wl
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
