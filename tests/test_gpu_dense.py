@@ -22,14 +22,3 @@ def test_dense_small(T, d, H):
     moe.check_device_error(DEV)
     ref, _ = O.dense_swiglu(inp.x, inp.w13, inp.w13_s, inp.w2, inp.w2_s)
     assert_close_layer(y, ref, what="dense")
-
-
-def test_dense_kimi_sampled():
-    shape = S.DENSE
-    inp = S.gen_dense_inputs(shape, seed=0, device=DEV)
-    y = moe.dense_swiglu_fp8(inp.x, inp.w13, inp.w13_s, inp.w2, inp.w2_s)
-    torch.cuda.synchronize()
-    moe.check_device_error(DEV)
-    toks = np.array([0, 1, 4095, 8191])
-    ref, _ = O.dense_swiglu(inp.x.cpu()[toks], inp.w13.cpu(), inp.w13_s.cpu(), inp.w2.cpu(), inp.w2_s.cpu())
-    assert_close_layer(y.cpu()[toks], ref, what="dense kimi")

@@ -16,29 +16,10 @@ import torch
 import moe_synth as S
 import routed_fp8_expert_gb300 as moe
 from oracle import moe_oracle as O
+from _hmargin import clear_of_midpoint, quotients
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-
-# e4m3 magnitudes in code order (codes 0x00..0x7E) and the midpoints between neighbours
-_MAGS = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
-_MIDS = (_MAGS[1:] + _MAGS[:-1]) / 2
-
-
-def _midpoint_distance(r: np.ndarray) -> np.ndarray:
-    """Distance of |r| to the nearest e4m3 rounding midpoint (in units of the quotient)."""
-    a = np.abs(r)
-    i = np.clip(np.searchsorted(_MIDS, a), 1, len(_MIDS) - 1)
-    return np.minimum(np.abs(a - _MIDS[i - 1]), np.abs(a - _MIDS[i]))
-
-
-# How far the GPU's fp32 quotient h / s may sit from the oracle's: fp32 sums of the
-# per-K-block partials and an fp32 SiLU move it by at most ~4e-4 on shapes like these
-# (emulated in fp32 with K up to 7168), so a margin of 4e-3 plus 1e-5 of the quotient
-# leaves a factor of ten.
-def _clear_of_midpoint(r: np.ndarray) -> np.ndarray:
-    return _midpoint_distance(r) > 4e-3 + 1e-5 * np.abs(r)
-
 
 def _run(shape, seed, zero_tokens=()):
     inp = S.gen_moe_inputs(shape, seed=seed)
@@ -74,10 +55,7 @@ def _run(shape, seed, zero_tokens=()):
         np.testing.assert_allclose(s[nz], s_ref[nz], rtol=1e-5, err_msg=f"expert {e}: scales")
         # codes: identical wherever the oracle's quotient h / s is clear of an e4m3
         # rounding midpoint; next to one, the neighbouring code on the same side of zero
-        n, H = q.shape
-        s_div = np.where(nz, s_ref, np.float32(1)).astype(np.float32)
-        ratio = (h_ref.reshape(n, H // 128, 128) / s_div[:, :, None]).astype(np.float32).reshape(n, H)
-        clear = _clear_of_midpoint(ratio.astype(np.float64))
+        clear = clear_of_midpoint(quotients(h_ref, s_ref).astype(np.float64))
         diff = q != q_ref
         assert not (diff & clear).any(), f"expert {e}: {int((diff & clear).sum())} codes differ away from a midpoint"
         mag, mag_ref = (q & 0x7F).astype(int), (q_ref & 0x7F).astype(int)
