@@ -126,7 +126,9 @@ int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx,
  *    n_shared <= 4; larger calls return MOE_ERR_UNSUPPORTED and enqueue nothing;
  *  - the first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture;
+ *    before any stream capture. The address is kept for the rest of the
+ *    process: calls after a cudaDeviceReset of that device are not supported
+ *    (the array may then live elsewhere);
  *  - every call on a device shares the array: calls that may run at the same
  *    time on the GPU (different streams without ordering) race and give wrong
  *    results. Nothing in the array needs to be zero between calls;
@@ -220,6 +222,17 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s,
  * mbarrier gave up since the last check (its outputs are then invalid);
  * MOE_OK otherwise. *detail (may be NULL) receives the raw error bits. */
 int moe_check_device_error(void *stream, uint32_t *detail);
+
+/* Self-test of the kernels' bounded waits (test only; the pages have no
+ * counterpart). Enqueues one small kernel whose two warps wait, through the
+ * grouped GEMMs' own wait routine, on a barrier that nothing ever completes: one
+ * with limit_ns (1000 .. 1e9 nanoseconds), the other with the kernels' usual 1 s
+ * limit. The first gives up after limit_ns, raises the CTA's abort word and sets
+ * bit 0x40 of the device error word; the second sees the abort word and returns.
+ * Nothing faults or traps and the context stays usable: the following
+ * moe_check_device_error returns MOE_ERR_TIMEOUT with detail 0x40, the one after
+ * it MOE_OK. MOE_ERR_ARG for a limit outside the range (nothing enqueued). */
+int moe_test_wait_timeout(uint64_t limit_ns, void *stream);
 
 /* Description of the calling thread's last error (static storage). */
 const char *moe_last_error_string(void);

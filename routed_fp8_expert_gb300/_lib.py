@@ -50,6 +50,7 @@ _SIGS = {
     "dense_swiglu_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "dense_swiglu_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_size, _vp]),
     "moe_check_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_test_wait_timeout": (_c_int, [ctypes.c_uint64, _vp]),
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_last_launch_count": (_c_int, []),
 }
@@ -277,6 +278,12 @@ def dense_swiglu_fp8(x, w13, w13_s, w2, w2_s, ws=None, y=None):
     _check(load().dense_swiglu_fp8(_p(x), _p(w13), _p(w13_s), _p(w2), _p(w2_s), d, H, T, _p(y), _p(ws),
                                    ws.numel(), _stream(dev)))
     return y
+
+
+def test_wait_timeout(limit_ns: int, device=None):
+    """moe_test_wait_timeout: the bounded-wait self-test (see the header); raises on
+    a bad limit. Read the result with check_device_error."""
+    _check(load().moe_test_wait_timeout(int(limit_ns), _stream(device)))
 
 
 def check_device_error(device=None):

@@ -84,14 +84,14 @@ int num_sms() {
 }
 
 // Token-tile width of the expert GEMMs: expected rows per routed expert k*T/E
-// decides. Narrow tiles leave more shared memory to the weight pipeline; the
-// 64-token tile keeps every TMEM chunk of a K block in registers at once.
+// decides.
 //
 // Decode regime (<= 12 expected rows per expert): 32-token tiles in the swap-AB
-// kernels (weight rows on the MMA M dimension) and the fused gate/up kernel,
-// which streams the weights at the HBM rate. Beyond it: 128-token tiles in the
-// token-major kernels (tokens on M), with gate and up as separate items of the
-// single-projection kernel, followed by the SwiGLU + quantise kernel.
+// kernels (weight rows on the MMA M dimension), the fused gate/up kernel and the
+// two-block down kernel, which stream the weights at the HBM rate. Beyond it:
+// 128-token tiles in the token-major kernels (tokens on M): gate/up items hold the
+// gate and up blocks of 128 features (N = 256) with the fused SiLU*mul and h
+// quantisation; down items hold two adjacent 128-row output blocks.
 bool decode_regime(const moe_cfg_t &c, int T) { return static_cast<double>(c.topk) * T / c.E <= 12.0; }
 
 int expert_bn(const moe_cfg_t &c, int T) { return decode_regime(c, T) ? 32 : 128; }
@@ -750,6 +750,15 @@ int moe_check_device_error(void *stream, uint32_t *detail) {
     if (v) MOE_CUDA(cudaMemset(word, 0, sizeof(v)), "error word clear");
     if (detail) *detail = v;
     if (v) return fail(MOE_ERR_TIMEOUT, "device error bits 0x%x (a bounded wait gave up)", v);
+    return MOE_OK;
+}
+
+int moe_test_wait_timeout(uint64_t limit_ns, void *stream) {
+    t_launches = 0;
+    if (limit_ns < 1000 || limit_ns > 1000000000ull)
+        return fail(MOE_ERR_ARG, "limit_ns=%llu must be in [1000, 1e9]", static_cast<unsigned long long>(limit_ns));
+    MOE_CUDA(launch_wait_selftest(limit_ns, static_cast<cudaStream_t>(stream)), "wait self-test launch");
+    t_launches = 1;
     return MOE_OK;
 }
 

@@ -712,9 +712,10 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                         // correctly rounded, then q0 + (h - sq q0) r, the inner term exact
                         // by FMA. For sq >= 2^-80 an underflowing term can only touch
                         // quotients below 2^-11, under every e4m3 rounding boundary, so the
-                        // codes are those of IEEE division; smaller scales divide.
+                        // codes are those of IEEE division; smaller scales, and an
+                        // infinite or NaN one, divide.
                         uint32_t w[FPT / 4];
-                        if (sq >= 8.27180613e-25f) {   // 2^-80
+                        if (sq >= 8.27180613e-25f && sq <= 3.40282347e38f) {   // 2^-80 <= sq <= FLT_MAX
                             const float rq = 1.0f / sq;
                             auto qd = [&](float x) -> float {
                                 const float q0 = x * rq;

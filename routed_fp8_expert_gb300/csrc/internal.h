@@ -62,6 +62,7 @@ cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos
                            void *y, cudaStream_t stream);
 cudaError_t launch_rmsnorm_quant(const void *h, const void *gamma, float eps, int rows, int cols, void *y,
                                  uint8_t *q, float *s, bool s_transposed, cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_combine_residual_rmsnorm(const void *o, const float *w, const int32_t *inv_pos, int T, int k,
                                             int S, int d, const void *residual, const void *gamma, float eps,
                                             void *h_out, void *x_next, cudaStream_t stream);

@@ -67,6 +67,13 @@ cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos
                       inv_pos, T, k, S, d, static_cast<__nv_bfloat16 *>(y));
 }
 
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(wait_selftest_kernel, dim3(1), dim3(64), 0, stream, err, limit_ns);
+}
+
 // Threads of a one-row-per-CTA kernel: kRowUnits 8-element units each, a multiple
 // of 32, at most 1024 (longer rows loop). A d = 7168 row: 224 threads.
 static int row_threads(int cols) {

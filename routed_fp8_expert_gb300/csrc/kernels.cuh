@@ -27,11 +27,12 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&v)[8]) {
 // x / s when no step over- or underflows. The quotients here are at most 448 in
 // magnitude. For s >= 2^-80, e can lose bits to underflow only where the quotient
 // lies below 2^-11, under every e4m3 rounding boundary, so the codes equal those
-// of IEEE division. A zero quotient takes x's sign, as x / s does. Smaller scales
-// fall back to the division.
+// of IEEE division. A zero quotient takes x's sign, as x / s does. Smaller scales,
+// and an infinite or NaN scale (a group holding an infinity or a NaN, where the
+// correction term would be NaN), fall back to the division.
 template <int N>
 __device__ __forceinline__ void div_by_scale(const float (&x)[N], float s, float (&q)[N]) {
-    if (s >= 8.27180613e-25f) {   // 2^-80
+    if (s >= 8.27180613e-25f && s <= 3.40282347e38f) {   // 2^-80 <= s <= FLT_MAX
         const float r = 1.0f / s;
 #pragma unroll
         for (int i = 0; i < N; ++i) {
@@ -479,6 +480,28 @@ __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float 
 #pragma unroll
     for (int i = 0; i < 4; ++i) oh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
     reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * d)[v] = out;
+}
+
+// ------------------------------------------------------------------ bounded-wait self-test
+// One CTA of two warps whose lane 0s wait on an mbarrier that nothing arrives at,
+// through the GEMMs' own bounded wait: warp 0 with the given limit, warp 1 with the
+// kernels' usual limit. Warp 0 gives up, raises the CTA's abort word and records
+// ERR_WAIT_SELFTEST; warp 1 sees the abort word and returns without recording.
+// No trap, no fault: the context stays usable.
+__global__ void wait_selftest_kernel(unsigned int *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_word;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_word = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0)
+        mbar_wait_for(smem_u32(&bar), 0, smem_u32(&abort_word), err, ERR_WAIT_SELFTEST,
+                      warp == 0 ? limit_ns : kWaitLimitNs);
+    __syncthreads();
 }
 
 // ------------------------------------------------------------------ block pieces

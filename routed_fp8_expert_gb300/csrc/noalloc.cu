@@ -43,7 +43,9 @@ static __device__ __align__(256) int32_t g_permute_scratch[kScratchWords];
 namespace {
 
 // Device address of the scratch array on the current device, looked up once
-// per device. The host-side name g_permute_scratch is only a stand-in for it.
+// per device and kept for the process (after a cudaDeviceReset the module, and
+// the array with it, may load elsewhere: calls after one are not supported). The
+// host-side name g_permute_scratch is only a stand-in for the address.
 int32_t *scratch_on_current_device() {
     static std::mutex mu;
     static int32_t *addr[64] = {nullptr};

@@ -15,6 +15,7 @@ enum : uint32_t {
     ERR_WAIT_PART_EMPTY = 1u << 3, // MMA issuer waited too long for the epilogue
     ERR_WAIT_DRAIN = 1u << 4,      // draining in-flight copies / MMAs timed out
     ERR_BAD_TILE = 1u << 5,        // a schedule entry was out of range (skipped)
+    ERR_WAIT_SELFTEST = 1u << 6,   // the bounded-wait self-test gave up, as it must
 };
 
 // Upper bound of any single wait inside one kernel (nanoseconds of %globaltimer).
@@ -104,21 +105,28 @@ __device__ __forceinline__ void st_volatile_shared(uint32_t addr, int v) {
 
 // Wait until the phase with the given parity has completed. Gives up when the
 // shared abort word at `abort_addr` becomes non-zero (another role gave up) or
-// after kWaitLimitNs, in which case it raises the abort word and records
-// `err_bit`. Returns false on give-up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t abort_addr,
-                                          unsigned int *err, uint32_t err_bit) {
+// after `limit_ns`, in which case it raises the abort word and records
+// `err_bit`. Returns false on give-up. Suspensions are capped at limit_ns too.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint32_t abort_addr,
+                                              unsigned int *err, uint32_t err_bit, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
+    const uint32_t sleep_ns = limit_ns < kWaitSleepNs ? static_cast<uint32_t>(limit_ns) : kWaitSleepNs;
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
         if (ld_volatile_shared(abort_addr)) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             st_volatile_shared(abort_addr, 1);
             record_error(err, err_bit);
             return false;
         }
     }
+}
+
+// mbar_wait_for with the kernels' limit, kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t abort_addr,
+                                          unsigned int *err, uint32_t err_bit) {
+    return mbar_wait_for(bar, parity, abort_addr, err, err_bit, kWaitLimitNs);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight work).

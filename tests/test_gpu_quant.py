@@ -139,3 +139,37 @@ def test_quantiser_division_midpoints_across_scales():
     qo, so = O.quantize_1x128(x)
     np.testing.assert_array_equal(s.view(np.uint32), so.view(np.uint32))
     np.testing.assert_array_equal(q, qo)
+
+
+def _same_codes_up_to_nan_sign(q, qo):
+    """Codes equal, except that a NaN code (S.1111.111) may carry either sign: the
+    sign of a NaN produced by an invalid operation differs between machines."""
+    nan, nan_o = (q & 0x7F) == 0x7F, (qo & 0x7F) == 0x7F
+    np.testing.assert_array_equal(nan, nan_o)
+    np.testing.assert_array_equal(q[~nan], qo[~nan])
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_nan_and_infinity_groups(bf16):
+    # a NaN in a group makes its amax and scale NaN and every quotient NaN; an
+    # infinity makes the scale infinite, its own quotient NaN (inf / inf) and the
+    # group's finite quotients +-0 (x / inf); other groups are unaffected
+    rows, cols = 6, 512
+    x = torch.randn(rows, cols, generator=torch.Generator().manual_seed(7)) * 2
+    x[0, 3] = float("nan")
+    x[1, 130] = float("inf")
+    x[2, 260] = float("-inf")
+    x[3, 0], x[3, 129] = float("inf"), float("nan")
+    x[4, 384:] = float("inf")
+    if bf16:
+        x = x.to(torch.bfloat16)
+    q, s = _run(x)
+    qo, so = O.quantize_1x128(x.float().numpy())
+    _same_codes_up_to_nan_sign(q, qo)
+    np.testing.assert_array_equal(np.isnan(s), np.isnan(so))
+    fin = ~np.isnan(so)
+    np.testing.assert_array_equal(s[fin], so[fin])
+    # the groups with an infinity: scale +inf, finite elements quantise to +-0
+    assert np.isinf(s[1, 1]) and (q[1, 128:256][np.arange(128) != 2] & 0x7F == 0).all()
+    # groups untouched by the special values are those of the plain quantiser
+    assert (q[5] == qo[5]).all() and (s[5] == so[5]).all()
