@@ -470,6 +470,7 @@ def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
     e2e_value = tokens_total / (e2e_ms * 1e-3)
     same = torch.equal(yd, y)
     pieces = time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks)
+    pieces["moe_block_ffn_forward"] = time_block_call(moe, x, wg, b, ex, cfg, ws, dev, n=max(3, min(args.steps, 20)))
     step_bytes = layer_weight_bytes + 2 * T * d * 2
 
     line = {
@@ -534,6 +535,35 @@ def time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks, n=50):
         ms = e0.elapsed_time(e1) / n
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"ms": ms, "alg_bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    return out
+
+
+def time_block_call(moe, x, wg, b, ex, cfg, ws, dev, n=20):
+    """The FFN half of the block in one call (RMSNorm_post with the fused
+    quantisation, the layer, residual addition and RMSNorm_next) against the
+    one-call layer on the same inputs (x as the residual stream): CUDA events, n
+    calls each after three warm-up calls."""
+    g_post = S.gen_norm_weight(x.shape[1], seed=1, name="norm_post", device=dev)
+    g_next = S.gen_norm_weight(x.shape[1], seed=1, name="norm_next", device=dev)
+    h_out = torch.empty_like(x)
+    x_next = torch.empty_like(x)
+    y = torch.empty_like(x)
+    calls = {"block_ms": lambda: moe.block_ffn_forward(x, g_post, wg, b, ex, cfg, gamma_next=g_next, ws=ws,
+                                                        h_out=h_out, x_next=x_next),
+             "layer_ms": lambda: moe.layer_forward(x, wg, b, ex, cfg, ws=ws, y=y)}
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        out[name] = e0.elapsed_time(e1) / n
+    out["extra_ms"] = out["block_ms"] - out["layer_ms"]
     return out
 
 

@@ -204,6 +204,24 @@ int moe_layer_forward(const void *x, const void *w_gate, const float *bias,
                       const moe_cfg_t *cfg, int T, void *y, int32_t *topk_idx, float *topk_w,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* The FFN half of a MoE block in one call ("Kimi K2 · Dense transformer block",
+ * Sources: residual = h; h = post_attention_layernorm(h); h = mlp(h);
+ * h = residual + h; "Kimi-K2-Base", Normalization and stability: RMSNorm, eps):
+ *   x      = RMSNorm_post(h) = bf16(gamma_post * h / sqrt(mean(h^2) + eps)),
+ *            with its 1x128 e4m3 codes and scales formed in the same pass (the
+ *            layer's input quantisation, bit for bit that of moe_quant_fp8_1x128
+ *            on x; no second pass over x);
+ *   y      = the MoE layer of moe_layer_forward on x (route on x, permute the codes);
+ *   h_out  = bf16(h + bf16(y));
+ *   x_next = RMSNorm_next(h_out) when gamma_next is given (the next block's input).
+ * h [T, d] bf16 (the residual stream), gamma_post / gamma_next [d] bf16, eps >= 0;
+ * h_out, x_next [T, d] bf16 (gamma_next and x_next both given or both NULL);
+ * other arguments as in moe_layer_forward; workspace: moe_workspace_bytes(cfg, T). */
+int moe_block_ffn_forward(const void *h, const void *gamma_post, float eps, const void *w_gate, const float *bias,
+                          const uint8_t *w13, const float *w13_s, const uint8_t *w2, const float *w2_s,
+                          const moe_cfg_t *cfg, int T, const void *gamma_next, void *h_out, void *x_next,
+                          int32_t *topk_idx, float *topk_w, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of workspace for dense_swiglu_fp8. Host only. */
 size_t dense_swiglu_workspace_bytes(int d, int H, int T);
 

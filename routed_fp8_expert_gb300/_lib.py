@@ -47,6 +47,8 @@ _SIGS = {
                                               ctypes.c_float, _vp, _vp, _vp]),
     "moe_layer_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp,
                                    _vp, _vp, _c_size, _vp]),
+    "moe_block_ffn_forward": (_c_int, [_vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "dense_swiglu_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "dense_swiglu_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_size, _vp]),
     "moe_check_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
@@ -262,6 +264,27 @@ def layer_forward(x, w_gate, bias, experts, cfg: MoeCfg, ws=None, y=None, want_r
                                     _p(experts.w2), _p(experts.w2_s), ctypes.byref(cfg), T, _p(y), _p(idx), _p(w),
                                     _p(ws), ws.numel(), _stream(dev)))
     return (y, idx, w) if want_routing else y
+
+
+def block_ffn_forward(h, gamma_post, w_gate, bias, experts, cfg: MoeCfg, gamma_next=None,
+                      eps: float = RMS_NORM_EPS, ws=None, h_out=None, x_next=None, want_routing=False):
+    """moe_block_ffn_forward: RMSNorm_post(h) -> the MoE layer -> h + y -> RMSNorm_next.
+    Returns (h_out, x_next or None) (and topk_idx, topk_w when want_routing)."""
+    _cuda(h, gamma_post, w_gate, bias, experts.w13, gamma_next)
+    T = h.shape[0]
+    dev = h.device
+    h_out = torch.empty((T, cfg.d), dtype=torch.bfloat16, device=dev) if h_out is None else h_out
+    if gamma_next is not None and x_next is None:
+        x_next = torch.empty((T, cfg.d), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((T, cfg.topk), dtype=torch.int32, device=dev) if want_routing else None
+    w = torch.empty((T, cfg.topk), dtype=torch.float32, device=dev) if want_routing else None
+    ws = workspace(cfg, T, dev) if ws is None else ws
+    _check(load().moe_block_ffn_forward(_p(h), _p(gamma_post), float(eps), _p(w_gate), _p(bias), _p(experts.w13),
+                                        _p(experts.w13_s), _p(experts.w2), _p(experts.w2_s), ctypes.byref(cfg), T,
+                                        _p(gamma_next), _p(h_out), _p(x_next if gamma_next is not None else None),
+                                        _p(idx), _p(w), _p(ws), ws.numel(), _stream(dev)))
+    x_out = x_next if gamma_next is not None else None
+    return (h_out, x_out, idx, w) if want_routing else (h_out, x_out)
 
 
 def dense_workspace(d, H, T, device):

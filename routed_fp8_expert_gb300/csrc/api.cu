@@ -157,6 +157,7 @@ struct LayerWs {
     uint8_t *hq;
     float *hs_t;
     __nv_bfloat16 *o;
+    __nv_bfloat16 *xn;   // moe_block_ffn_forward: the post-attention RMSNorm of h (bf16)
     size_t bytes;
 };
 
@@ -188,6 +189,7 @@ LayerWs carve_layer(const moe_cfg_t &c, int T, void *base) {
     w.hq = cv.take<uint8_t>(R * c.H);
     w.hs_t = cv.take<float>(R * (c.H / 128) * 4);
     w.o = cv.take<__nv_bfloat16>(R * c.d * 2);
+    w.xn = cv.take<__nv_bfloat16>(Tz * c.d * 2);
     w.bytes = align_up(cv.off, 1024);
     return w;
 }
@@ -659,6 +661,65 @@ int moe_layer_forward(const void *x, const void *w_gate, const float *bias, cons
     MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, false, st));
     n += t_launches;
     MOE_CUDA(launch_combine(ws.o, w, ws.inv_pos, T, c.topk, c.n_shared, c.d, y, st), "combine launch");
+    n += 1;
+    t_launches = n;
+    return MOE_OK;
+}
+
+int moe_block_ffn_forward(const void *h, const void *gamma_post, float eps, const void *w_gate, const float *bias,
+                          const uint8_t *w13, const float *w13_s, const uint8_t *w2, const float *w2_s,
+                          const moe_cfg_t *cfg, int T, const void *gamma_next, void *h_out, void *x_next,
+                          int32_t *topk_idx, float *topk_w, void *workspace, size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (!(eps >= 0.f)) return fail(MOE_ERR_ARG, "eps must be a non-negative number");
+    if ((gamma_next == nullptr) != (x_next == nullptr))
+        return fail(MOE_ERR_ARG, "gamma_next and x_next are both given or both NULL");
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(h, "h"));
+    MOE_CHECK(check_ptr(gamma_post, "gamma_post"));
+    MOE_CHECK(check_ptr(w_gate, "w_gate"));
+    if (!bias) return fail(MOE_ERR_ARG, "bias is NULL");
+    MOE_CHECK(check_ptr(w13, "w13"));
+    MOE_CHECK(check_ptr(w13_s, "w13_s"));
+    MOE_CHECK(check_ptr(w2, "w2"));
+    MOE_CHECK(check_ptr(w2_s, "w2_s"));
+    MOE_CHECK(check_ptr(h_out, "h_out"));
+    if (gamma_next) {
+        MOE_CHECK(check_ptr(gamma_next, "gamma_next"));
+        MOE_CHECK(check_ptr(x_next, "x_next"));
+    }
+    if (topk_idx) MOE_CHECK(check_ptr(topk_idx, "topk_idx"));
+    if (topk_w) MOE_CHECK(check_ptr(topk_w, "topk_w"));
+    const moe_cfg_t &c = *cfg;
+    const LayerWs need = carve_layer(c, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(c, T, workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t *idx = topk_idx ? topk_idx : ws.idx;
+    float *w = topk_w ? topk_w : ws.w;
+    int n = 0;
+    // x = RMSNorm_post(h) in bf16 for the router, and its 1x128 codes and scales in
+    // the same pass: the layer's input quantisation, not repeated
+    MOE_CUDA(launch_rmsnorm_quant(h, gamma_post, eps, T, c.d, ws.xn, ws.xq, ws.sx, false, st),
+             "RMSNorm quantise launch");
+    n += 1;
+    MOE_CHECK(route_impl(ws.xn, w_gate, bias, c, T, idx, w, nullptr, ws.logits, st));
+    n += t_launches;
+    int np = 0;
+    MOE_CUDA(launch_permute(idx, ws.xq, ws.sx, T, c.topk, c.n_shared, c.E, c.d, expert_bn(c, T), down_bn(c, T),
+                            ws.rank, ws.cnt, ws.counts, ws.offsets, ws.row_start, ws.tile_prefix, ws.tile_prefix_dn,
+                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st),
+             "permutation launch");
+    n += np;
+    t_launches = 0;
+    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, false, st));
+    n += t_launches;
+    // h_out = h + y (y rounded to bf16), x_next = RMSNorm_next(h_out)
+    MOE_CUDA(launch_combine_residual_rmsnorm(ws.o, w, ws.inv_pos, T, c.topk, c.n_shared, c.d, h, gamma_next, eps,
+                                             h_out, x_next, st),
+             "combine + residual + RMSNorm launch");
     n += 1;
     t_launches = n;
     return MOE_OK;

@@ -158,3 +158,79 @@ def _close_bf16(got, ref, abs_tol, what):
     bound = abs_tol + 2.0 * _ulp_bf16(ref)
     assert (err <= bound).all(), f"{what}: max excess {(err - bound).max():.3e}"
     assert err.mean() / np.abs(ref).mean() <= 5e-3, f"{what}: mean relative error {err.mean() / np.abs(ref).mean():.2e}"
+
+
+def _split_chain(h, g_post, wg, b, ex, cfg, T, g_next):
+    """The block's FFN half through the separate calls."""
+    x, xq, sx = moe.rmsnorm_quant_fp8(h, g_post)
+    idx, w, _ = moe.route(x, wg, b, cfg)
+    offs, st, inv, xqp, sxp = moe.permute(idx, xq, sx, cfg)
+    o = moe.expert_gemm_fp8(xqp, sxp, offs, ex, cfg, T)
+    h_next, x_next = moe.combine_residual_rmsnorm(o, w, inv, cfg, T, h, g_next)
+    return h_next, x_next, idx
+
+
+def test_block_ffn_one_call_toy():
+    # moe_block_ffn_forward: the same bits as the chain of separate calls (its
+    # pieces are those calls' kernels, with the RMSNorm pass's codes feeding the
+    # permutation), and the oracle's moe_block_ffn within the tolerances above
+    shape = S.TOY
+    inp = S.gen_moe_inputs(shape, seed=12)
+    h = S.gen_residual(shape.T, shape.d, seed=12, std=0.05)
+    g_post = S.gen_norm_weight(shape.d, seed=12, name="norm_post")
+    g_next = S.gen_norm_weight(shape.d, seed=12, name="norm_next")
+    cfg = moe.cfg_of(shape)
+    ex = inp.experts.to(DEV)
+    hd, gp, gn, wg, b = (t.to(DEV) for t in (h, g_post, g_next, inp.w_gate, inp.bias))
+    h_next, x_next, idx, w = moe.block_ffn_forward(hd, gp, wg, b, ex, cfg, gamma_next=gn, want_routing=True)
+    h_only, none = moe.block_ffn_forward(hd, gp, wg, b, ex, cfg)
+    h_ref_chain, x_ref_chain, idx_chain = _split_chain(hd, gp, wg, b, ex, cfg, shape.T, gn)
+    torch.cuda.synchronize()
+    moe.check_device_error(DEV)
+    assert moe.last_launch_count() >= 1 and none is None
+    assert torch.equal(idx, idx_chain)
+    assert torch.equal(h_next, h_ref_chain) and torch.equal(x_next, x_ref_chain) and torch.equal(h_only, h_next)
+    x_ref = O.rms_norm(h, g_post, EPS).astype(np.float32)
+    r = O.route(x_ref, inp.w_gate.float().numpy(), inp.bias.double().numpy(), shape.topk, shape.route_scale)
+    use_idx = reconcile_routing(idx.cpu().numpy(), r, shape.topk)
+    ref = O.moe_block_ffn(h, g_post, inp.w_gate, inp.bias, inp.experts, shape.topk, shape.route_scale,
+                          gamma_next=g_next, idx_override=use_idx)
+    y_rms = np.sqrt((ref["y"] ** 2).mean())
+    _close_bf16(h_next.float().cpu().numpy(), ref["h_next"], 2e-2 * y_rms, "h_next")
+    x_rms = np.sqrt((ref["x_next"] ** 2).mean())
+    _close_bf16(x_next.float().cpu().numpy(), ref["x_next"], 2e-2 * x_rms, "x_next")
+
+
+def test_block_ffn_one_call_kimi_decode():
+    # the Kimi K2 decode batch (T=256, d=7168, 384 experts): the one call equals the
+    # chain of separate calls bit for bit, and the oracle on three tokens
+    shape = S.DECODE
+    T, d = shape.T, shape.d
+    ex = S.gen_experts(shape.E + 1, d, shape.H, seed=0, device=DEV)
+    wg, b = S.gen_router(shape, seed=4, device=DEV)
+    h = S.gen_residual(T, d, seed=4, std=1.0, device=DEV)
+    g_post = S.gen_norm_weight(d, seed=4, name="norm_post", device=DEV)
+    g_next = S.gen_norm_weight(d, seed=4, name="norm_next", device=DEV)
+    cfg = moe.cfg_of(shape)
+    h_next, x_next, idx, w = moe.block_ffn_forward(h, g_post, wg, b, ex, cfg, gamma_next=g_next, want_routing=True)
+    h_chain, x_chain, idx_chain = _split_chain(h, g_post, wg, b, ex, cfg, T, g_next)
+    torch.cuda.synchronize()
+    moe.check_device_error(DEV)
+    assert torch.equal(idx, idx_chain) and torch.equal(h_next, h_chain) and torch.equal(x_next, x_chain)
+    hc = h.cpu()
+    x_ref = O.rms_norm(hc, g_post.cpu(), EPS).astype(np.float32)
+    r = O.route(x_ref, wg.cpu().float().numpy(), b.cpu().double().numpy(), shape.topk, shape.route_scale)
+    use_idx = reconcile_routing(idx.cpu().numpy(), r, shape.topk)
+    toks = [0, 97, T - 1]
+    need = sorted(set(use_idx[toks].ravel().tolist()) | {shape.E})
+    host = S.ExpertWeights(*(torch.zeros((shape.E + 1,) + t.shape[1:], dtype=t.dtype)
+                             for t in (ex.w13, ex.w13_s, ex.w2, ex.w2_s)))
+    for e in need:
+        host.w13[e].copy_(ex.w13[e].cpu()); host.w13_s[e].copy_(ex.w13_s[e].cpu())
+        host.w2[e].copy_(ex.w2[e].cpu()); host.w2_s[e].copy_(ex.w2_s[e].cpu())
+    ref = O.moe_block_ffn(hc, g_post.cpu(), wg.cpu(), b.cpu(), host, shape.topk, shape.route_scale,
+                          gamma_next=g_next.cpu(), tokens=toks, idx_override=use_idx)
+    y_rms = np.sqrt((ref["y"][toks] ** 2).mean())
+    _close_bf16(h_next.float().cpu().numpy()[toks], ref["h_next"][toks], 2e-2 * y_rms, "h_next")
+    x_rms = np.sqrt((ref["x_next"][toks] ** 2).mean())
+    _close_bf16(x_next.float().cpu().numpy()[toks], ref["x_next"][toks], 2e-2 * x_rms, "x_next")
