@@ -52,7 +52,9 @@ typedef enum {
     MOE_ERR_ARG = -1,          /* null pointer, misaligned pointer, bad size or short workspace */
     MOE_ERR_UNSUPPORTED = -2,  /* shape outside the supported range */
     MOE_ERR_CUDA = -3,         /* a CUDA call or launch failed; see moe_last_error_string() */
-    MOE_ERR_TIMEOUT = -4       /* a bounded device wait gave up (reported by moe_check_device_error) */
+    MOE_ERR_TIMEOUT = -4,      /* a bounded device wait gave up (reported by moe_check_device_error) */
+    MOE_ERR_INDEX = -5         /* a device-side index check failed and its access was skipped
+                                  (reported by moe_check_device_error) */
 } moe_status_t;
 
 /* Shape of one MoE layer. */
@@ -237,8 +239,12 @@ int dense_swiglu_fp8(const void *x, const uint8_t *w13, const float *w13_s,
 
 /* Reads and clears the device error word of the current device after
  * synchronising `stream`. MOE_ERR_TIMEOUT if a kernel's bounded wait on an
- * mbarrier gave up since the last check (its outputs are then invalid);
- * MOE_OK otherwise. *detail (may be NULL) receives the raw error bits. */
+ * mbarrier gave up since the last check (bits 0x01..0x10, 0x40; its outputs are
+ * then invalid); otherwise MOE_ERR_INDEX if an index check failed and the
+ * access was skipped (0x20: a GEMM work item outside the schedule; 0x80, the
+ * bounds-checked build only: an expert id, a permuted position or an item's
+ * rows outside their buffer); MOE_OK if no bit is set. *detail (may be NULL)
+ * receives the raw error bits. */
 int moe_check_device_error(void *stream, uint32_t *detail);
 
 /* Self-test of the kernels' bounded waits (test only; the pages have no

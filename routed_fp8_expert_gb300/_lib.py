@@ -15,7 +15,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_fp8.so")
 
-MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = 0, -1, -2, -3, -4
+MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_INDEX = 0, -1, -2, -3, -4, -5
 
 _c_int, _c_size, _c_i64, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_int64, ctypes.c_void_p
 

@@ -2,6 +2,9 @@
 
 Each translation unit under csrc/ compiles in parallel to an object file in
 _build/, then nvcc links them (static CUDA runtime) into the package folder.
+build(debug_bounds=True) builds the bounds-checked variant libmoe_fp8_debug.so
+(-DMOE_DEBUG_BOUNDS, objects in _build_debug/): every index that addresses a
+buffer row is checked, and a bad one is recorded and its access skipped.
 """
 from __future__ import annotations
 
@@ -17,6 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_fp8.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libmoe_fp8_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]
@@ -41,13 +46,16 @@ def _deps_newer(obj: str) -> bool:
     return any(os.path.getmtime(p) > t for p in deps) or os.path.getmtime(__file__) > t
 
 
-def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_verbose: bool = False, debug_bounds: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug_bounds else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if debug_bounds:
+        extra.append("-DMOE_DEBUG_BOUNDS")
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if not ptxas_verbose and not _deps_newer(obj):
             return obj, ""
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
@@ -62,13 +70,13 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
         if log and (verbose or ptxas_verbose):
             print(log, file=sys.stderr)
     objs = [o for o, _ in results]
-    if not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
+    if not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        cmd = [nvcc, *ARCH, "-shared", "-o", lib + ".tmp", *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -810,7 +810,10 @@ int moe_check_device_error(void *stream, uint32_t *detail) {
     MOE_CUDA(cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost), "error word read");
     if (v) MOE_CUDA(cudaMemset(word, 0, sizeof(v)), "error word clear");
     if (detail) *detail = v;
-    if (v) return fail(MOE_ERR_TIMEOUT, "device error bits 0x%x (a bounded wait gave up)", v);
+    if (v & (ERR_WAIT_TMA_FULL | ERR_WAIT_SMEM_EMPTY | ERR_WAIT_PART_FULL | ERR_WAIT_PART_EMPTY | ERR_WAIT_DRAIN |
+             ERR_WAIT_SELFTEST))
+        return fail(MOE_ERR_TIMEOUT, "device error bits 0x%x (a bounded wait gave up)", v);
+    if (v) return fail(MOE_ERR_INDEX, "device error bits 0x%x (an index check failed; its access was skipped)", v);
     return MOE_OK;
 }
 

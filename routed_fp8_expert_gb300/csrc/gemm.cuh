@@ -208,6 +208,8 @@ __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int
         o.ntiles = s_tp[g + 1] - s_tp[g];
     }
     o.mb = mbx;
+    // (bounds-checked build: an item's rows inside the activation buffer)
+    if (kDebugBounds && (o.row0 < 0 || o.row0 + o.n > a.total_rows)) return false;
     return o.n > 0 && o.mb < a.num_mb;
 }
 

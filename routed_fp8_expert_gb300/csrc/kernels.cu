@@ -35,8 +35,11 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
                            cudaStream_t stream) {
     const int C = (T + 31) / 32;
     const size_t smem = sizeof(uint32_t) * kPermWarps * E;
-    cudaError_t e = launch_pdl(perm_rank_kernel, dim3((C + kPermWarps - 1) / kPermWarps), dim3(kPermWarps * 32), smem,
-                               stream, idx, T, k, E, C, rank, cnt);
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(perm_rank_kernel, dim3((C + kPermWarps - 1) / kPermWarps), dim3(kPermWarps * 32), smem, stream, idx,
+                   T, k, E, C, rank, cnt, err);
     if (e != cudaSuccess) return e;
     e = launch_pdl(perm_scan_kernel, dim3(E), dim3(256), 0, stream, cnt, C, counts);
     if (e != cudaSuccess) return e;
@@ -45,7 +48,7 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
     if (e != cudaSuccess) return e;
     const int threads = min(1024, max(64, d / 16));
     e = launch_pdl(perm_scatter_kernel, dim3(T), dim3(threads), 0, stream, idx, rank, cnt, offsets, xq, sx, T, k, S,
-                   E, d, C, sorted_tok, inv_pos, xq_perm, sx_perm);
+                   E, d, C, sorted_tok, inv_pos, xq_perm, sx_perm, err);
     *launches += 4;
     return e;
 }
@@ -63,8 +66,11 @@ cudaError_t launch_combine(const void *o, const float *w, const int32_t *inv_pos
     const int units = d / 8;
     const int threads = 128;
     const dim3 grid(T, (units + threads - 1) / threads);
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) return e;
     return launch_pdl(combine_kernel, grid, dim3(threads), 0, stream, static_cast<const __nv_bfloat16 *>(o), w,
-                      inv_pos, T, k, S, d, static_cast<__nv_bfloat16 *>(y));
+                      inv_pos, T, k, S, d, static_cast<__nv_bfloat16 *>(y), err);
 }
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
@@ -97,9 +103,12 @@ cudaError_t launch_combine_residual_rmsnorm(const void *o, const float *w, const
     const int threads = row_threads(d);
     auto kernel = (threads <= 256 && T <= 512) ? combine_residual_rmsnorm_kernel<true>
                                                 : combine_residual_rmsnorm_kernel<false>;
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kernel, dim3(T), dim3(threads), 0, stream, static_cast<const __nv_bfloat16 *>(o), w, inv_pos, T,
                       k, S, d, static_cast<const __nv_bfloat16 *>(residual), static_cast<const __nv_bfloat16 *>(gamma),
-                      eps, static_cast<__nv_bfloat16 *>(h_out), static_cast<__nv_bfloat16 *>(x_next));
+                      eps, static_cast<__nv_bfloat16 *>(h_out), static_cast<__nv_bfloat16 *>(x_next), err);
 }
 
 }  // namespace moe

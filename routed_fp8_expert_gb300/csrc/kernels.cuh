@@ -198,7 +198,7 @@ constexpr int kPermWarps = 8;
 // lanes that chose it; ranks and counts are population counts of those words.
 // Ids outside [0, E) are skipped (rank -1), so bad input cannot write out of bounds.
 __global__ void perm_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int C,
-                                 int32_t *__restrict__ rank, int32_t *__restrict__ cnt) {
+                                 int32_t *__restrict__ rank, int32_t *__restrict__ cnt, unsigned int *err) {
     pdl_trigger();
     pdl_wait();
     extern __shared__ uint32_t s_bits[];  // [kPermWarps][E]
@@ -214,6 +214,7 @@ __global__ void perm_rank_kernel(const int32_t *__restrict__ idx, int T, int k, 
         for (int j = 0; j < k; ++j) {
             const int e = row[j];
             if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicOr(&bits[e], 1u << lane);
+            else if (kDebugBounds) record_error(err, ERR_BAD_INDEX);
         }
     }
     __syncwarp();
@@ -377,7 +378,7 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
                                     const uint8_t *__restrict__ xq, const float *__restrict__ sx, int T, int k,
                                     int S, int E, int d, int C, int32_t *__restrict__ sorted_tok,
                                     int32_t *__restrict__ inv_pos, uint8_t *__restrict__ xq_perm,
-                                    float *__restrict__ sx_perm) {
+                                    float *__restrict__ sx_perm, unsigned int *err) {
     pdl_trigger();
     pdl_wait();
     __shared__ int32_t s_pos[40];
@@ -391,7 +392,10 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
         int pos = -1;
         if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
             pos = offsets[e] + cnt_scan[static_cast<size_t>(e) * C + c] + rank[static_cast<size_t>(t) * k + j];
-            if (pos < 0 || pos >= k * T) pos = -1;
+            if (pos < 0 || pos >= k * T) {
+                if (kDebugBounds) record_error(err, ERR_BAD_INDEX);
+                pos = -1;
+            }
         }
         s_pos[j] = pos;
         inv_pos[static_cast<size_t>(t) * k + j] = pos;
@@ -421,14 +425,19 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
 // the slice [slice * 8 * blockDim.x, ...) of token t.
 __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w,
                                const int32_t *__restrict__ inv_pos, int T, int k, int S, int d,
-                               __nv_bfloat16 *__restrict__ y) {
+                               __nv_bfloat16 *__restrict__ y, unsigned int *err) {
     pdl_trigger();
     pdl_wait();
     __shared__ int32_t s_pos[32];
     __shared__ float s_w[32];
     const int t = blockIdx.x;
     if (threadIdx.x < k) {
-        s_pos[threadIdx.x] = inv_pos[static_cast<size_t>(t) * k + threadIdx.x];
+        int p = inv_pos[static_cast<size_t>(t) * k + threadIdx.x];
+        if (kDebugBounds && (p < -1 || p >= k * T)) {   // a routed row is one of the k*T
+            record_error(err, ERR_BAD_INDEX);
+            p = -1;
+        }
+        s_pos[threadIdx.x] = p;
         s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
     }
     __syncthreads();
@@ -640,7 +649,7 @@ template <bool kBatch>
 __global__ void __launch_bounds__(kBatch ? 256 : 1024, kBatch ? 2 : 1) combine_residual_rmsnorm_kernel(
     const __nv_bfloat16 *__restrict__ o, const float *__restrict__ w, const int32_t *__restrict__ inv_pos, int T,
     int k, int S, int d, const __nv_bfloat16 *__restrict__ residual, const __nv_bfloat16 *__restrict__ gamma,
-    float eps, __nv_bfloat16 *__restrict__ h_out, __nv_bfloat16 *__restrict__ x_next) {
+    float eps, __nv_bfloat16 *__restrict__ h_out, __nv_bfloat16 *__restrict__ x_next, unsigned int *err) {
     pdl_trigger();
     pdl_wait();
     __shared__ int32_t s_pos[32];
@@ -648,7 +657,12 @@ __global__ void __launch_bounds__(kBatch ? 256 : 1024, kBatch ? 2 : 1) combine_r
     __shared__ float red[33];
     const int t = blockIdx.x;
     if (threadIdx.x < k) {
-        s_pos[threadIdx.x] = inv_pos[static_cast<size_t>(t) * k + threadIdx.x];
+        int p = inv_pos[static_cast<size_t>(t) * k + threadIdx.x];
+        if (kDebugBounds && (p < -1 || p >= k * T)) {   // a routed row is one of the k*T
+            record_error(err, ERR_BAD_INDEX);
+            p = -1;
+        }
+        s_pos[threadIdx.x] = p;
         s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
     }
     __syncthreads();

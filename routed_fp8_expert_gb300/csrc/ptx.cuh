@@ -16,7 +16,18 @@ enum : uint32_t {
     ERR_WAIT_DRAIN = 1u << 4,      // draining in-flight copies / MMAs timed out
     ERR_BAD_TILE = 1u << 5,        // a schedule entry was out of range (skipped)
     ERR_WAIT_SELFTEST = 1u << 6,   // the bounded-wait self-test gave up, as it must
+    ERR_BAD_INDEX = 1u << 7,       // (bounds-checked build) an index outside its buffer (access skipped)
 };
+
+// The bounds-checked build (-DMOE_DEBUG_BOUNDS): every index that addresses a row
+// of a buffer (an expert id, a permuted position, a GEMM item's rows) is checked
+// against the buffer's extent before use; a bad one records ERR_BAD_INDEX in the
+// device error word and the access is skipped.
+#ifdef MOE_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
 
 // Upper bound of any single wait inside one kernel (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
