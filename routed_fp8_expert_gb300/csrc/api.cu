@@ -306,9 +306,17 @@ int route_impl(const void *x, const void *wg, const float *bias, const moe_cfg_t
     return MOE_OK;
 }
 
+// Activation rows gathered by the decode gate/up kernel itself (instead of the
+// permuted copy): the unpermuted codes [T][d] and scales [T][d/128] and sorted_tok.
+struct Gather {
+    const uint8_t *xq;
+    const float *sx;
+    const int32_t *sorted_tok;
+};
+
 int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets, const uint8_t *w13,
                 const float *w13_s, const moe_cfg_t &c, int T, uint8_t *hq, float *hs, const LayerWs &ws,
-                bool run_sched, cudaStream_t st) {
+                bool run_sched, cudaStream_t st, const Gather *gather = nullptr) {
     const int G = c.E + c.n_shared;
     const int64_t R = static_cast<int64_t>(c.topk + c.n_shared) * T;
     const int bn = expert_bn(c, T);
@@ -341,6 +349,13 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
         gu.hq = hq;
         gu.hs_t = hs;
         gu.item_counter = ws.counters;
+        if (gather) {
+            gu.gather_rows = gather->xq;
+            gu.gather_scales = gather->sx;
+            gu.row_token = gather->sorted_tok;
+            gu.n_routed = c.topk * T;
+            gu.n_tok = T;
+        }
         MOE_CUDA(launch_grouped_gemm(Kind::GateUp, bn, m13, mx, gu, num_sms(), st), "gate/up GEMM launch");
         t_launches += 1;
         return MOE_OK;
@@ -411,8 +426,8 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
 
 int experts_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets, const uint8_t *w13,
                  const float *w13_s, const uint8_t *w2, const float *w2_s, const moe_cfg_t &c, int T, void *o,
-                 const LayerWs &ws, bool run_sched, cudaStream_t st) {
-    MOE_CHECK(gateup_impl(xq_perm, sx_perm, offsets, w13, w13_s, c, T, ws.hq, ws.hs_t, ws, run_sched, st));
+                 const LayerWs &ws, bool run_sched, cudaStream_t st, const Gather *gather = nullptr) {
+    MOE_CHECK(gateup_impl(xq_perm, sx_perm, offsets, w13, w13_s, c, T, ws.hq, ws.hs_t, ws, run_sched, st, gather));
     return down_impl(ws.hq, ws.hs_t, offsets, w2, w2_s, c, T, o, ws, false, st);
 }
 
@@ -650,15 +665,20 @@ int moe_layer_forward(const void *x, const void *w_gate, const float *bias, cons
     n += t_launches;
     MOE_CUDA(launch_quant(x, true, T, c.d, ws.xq, ws.sx, false, num_sms(), st), "quantise launch");
     n += 1;
+    // decode regime: the gate/up kernel gathers the activation rows by sorted_tok,
+    // so the permutation writes no copy of them
+    const bool gather = decode_regime(c, T);
+    const Gather g{ws.xq, ws.sx, ws.sorted_tok};
     int np = 0;
     MOE_CUDA(launch_permute(idx, ws.xq, ws.sx, T, c.topk, c.n_shared, c.E, c.d, expert_bn(c, T), down_bn(c, T),
                             ws.rank, ws.cnt, ws.counts, ws.offsets, ws.row_start, ws.tile_prefix, ws.tile_prefix_dn,
-                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st),
+                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st, !gather),
              "permutation launch");
     n += np;
     t_launches = 0;
     // the permutation already wrote the GEMM schedule into the workspace
-    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, false, st));
+    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, false, st,
+                           gather ? &g : nullptr));
     n += t_launches;
     MOE_CUDA(launch_combine(ws.o, w, ws.inv_pos, T, c.topk, c.n_shared, c.d, y, st), "combine launch");
     n += 1;
@@ -707,14 +727,17 @@ int moe_block_ffn_forward(const void *h, const void *gamma_post, float eps, cons
     n += 1;
     MOE_CHECK(route_impl(ws.xn, w_gate, bias, c, T, idx, w, nullptr, ws.logits, st));
     n += t_launches;
+    const bool gather = decode_regime(c, T);   // as in moe_layer_forward
+    const Gather g{ws.xq, ws.sx, ws.sorted_tok};
     int np = 0;
     MOE_CUDA(launch_permute(idx, ws.xq, ws.sx, T, c.topk, c.n_shared, c.E, c.d, expert_bn(c, T), down_bn(c, T),
                             ws.rank, ws.cnt, ws.counts, ws.offsets, ws.row_start, ws.tile_prefix, ws.tile_prefix_dn,
-                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st),
+                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st, !gather),
              "permutation launch");
     n += np;
     t_launches = 0;
-    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, false, st));
+    MOE_CHECK(experts_impl(ws.xq_perm, ws.sx_perm, ws.offsets, w13, w13_s, w2, w2_s, c, T, ws.o, ws, false, st,
+                           gather ? &g : nullptr));
     n += t_launches;
     // h_out = h + y (y rounded to bf16), x_next = RMSNorm_next(h_out)
     MOE_CUDA(launch_combine_residual_rmsnorm(ws.o, w, ws.inv_pos, T, c.topk, c.n_shared, c.d, h, gamma_next, eps,

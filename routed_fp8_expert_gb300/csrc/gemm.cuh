@@ -141,7 +141,32 @@ struct GemmArgs {
     int k_splits;             // Router: K range split into this many partial sums (>= 1)
     unsigned int *err;        // device error word (bounded waits that gave up)
     int *item_counter;        // dynamic scheduler counter (zero at launch), or null for static order
+    // GateUp gathering its activation rows (null: rows of the permuted copy by TMA):
+    // permuted row p holds token tok(p) = row_token[p] for p < n_routed, else
+    // (p - n_routed) % n_tok (the shared experts' rows); its codes are
+    // gather_rows[tok][num_kb * 128] and its scales gather_scales[tok][num_kb]
+    const uint8_t *gather_rows;
+    const float *gather_scales;
+    const int *row_token;
+    int n_routed;
+    int n_tok;
 };
+
+// Token of permuted row p in the gathering mode.
+__device__ __forceinline__ int gather_token(const GemmArgs &a, int p) {
+    return p < a.n_routed ? a.row_token[p] : (p - a.n_routed) % a.n_tok;
+}
+
+// 16-byte asynchronous global -> shared copy (L2 only).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Orders this thread's later async-proxy reads of shared memory (the MMAs) after
+// the generic-proxy writes it has observed complete (cp.async copies).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 struct Item {
     int g, mb, row0, n, ks;
@@ -337,7 +362,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);    // the producer's expect_tx arrival (+ TMA bytes)
+            // the producer's expect_tx arrival (+ TMA bytes); gathering GateUp: plus one
+            // cp.async arrival per producer lane
+            mbar_init(smem_u32(&full[s]), (KIND == Kind::GateUp && args.gather_rows) ? 33 : 1);
             mbar_init(smem_u32(&empty[s]), 1);   // the MMA commit
         }
         for (int s = 0; s < C::kScaleSlots; ++s) {
@@ -405,8 +432,14 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     // copy); the slot's full barrier counts one arrival per lane.
     auto copy_scales = [&](const Item &I, int kb, int slot, const float *ws0, const float *ws1) {
         const uint32_t sdst = smem_u32(s_scale + slot * L::kScaleStride);
-        const float *src = args.act_scale_t + static_cast<size_t>(kb) * args.total_rows + I.row0;
-        for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
+        if (KIND == Kind::GateUp && args.gather_rows) {
+            // the tile's tokens' scales straight from the unpermuted [T][num_kb] array
+            for (int i = lane; i < I.n; i += 32)
+                cp_async_4(sdst + 4 * i, args.gather_scales + static_cast<size_t>(gather_token(args, I.row0 + i)) * args.num_kb + kb);
+        } else {
+            const float *src = args.act_scale_t + static_cast<size_t>(kb) * args.total_rows + I.row0;
+            for (int i = lane; i < I.n; i += 32) cp_async_4(sdst + 4 * i, src + i);
+        }
         if (lane == 0) {
             cp_async_4(sdst + 4 * BN, ws0 + kb);
             if constexpr (C::kATiles == 2) cp_async_4(sdst + 4 * (BN + 1), ws1 + kb);
@@ -456,7 +489,18 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             const int box_i = act_box_index(I.n);
             // full boxes count toward the transaction bytes, including rows and a
             // K block beyond the tensor, which the TMA unit fills with zeros
-            const uint32_t bytes = C::kKPS * (C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes);
+            uint32_t bytes = C::kKPS * (C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes);
+            // gathering GateUp: lane i copies the tile's row i (one token's 128-byte K
+            // block, eight 16-byte copies into its 128-byte-swizzled place); only the
+            // weights come by TMA. Rows past the tile's end stay as they are: their
+            // output columns are never stored, and no column depends on another row
+            const bool gather = (KIND == Kind::GateUp) && args.gather_rows != nullptr;
+            const uint8_t *grow = nullptr;
+            if (gather) {
+                bytes = C::kATiles * kATileBytes;
+                if (lane < I.n)
+                    grow = args.gather_rows + static_cast<size_t>(gather_token(args, I.row0 + lane)) * args.num_kb * kKBytes;
+            }
             const uint64_t pol_w = (I.ntiles > 1) ? pol_shared : pol_stream;
             int arow0;
             if constexpr (KIND == Kind::Router) {
@@ -473,7 +517,19 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 if (!w) { ok = false; break; }
                 const uint32_t fb = smem_u32(&full[stage]);
                 const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
-                if (lane == 0) {
+                if (gather) {
+                    if (grow) {
+                        const uint32_t dst = sbase + C::kAStageBytes + lane * kKBytes;
+                        const uint8_t *src = grow + static_cast<size_t>(kb) * kKBytes;
+#pragma unroll
+                        for (int c = 0; c < kKBytes / 16; ++c) cp_async_16(dst + ((c ^ (lane & 7)) << 4), src + 16 * c);
+                    }
+                    cp_async_arrive_noinc(fb);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(fb, bytes);
+                        tma_load_3d(sbase, &map_a, fb, kb * kKbElems, I.mb * kBM, 2 * I.g, pol_w);
+                    }
+                } else if (lane == 0) {
                     mbar_arrive_expect_tx(fb, bytes);
                     // weight tiles in one request (the TMA unit's request rate, not its
                     // bytes, bounds an SM's loads): GateUp's gate and up tiles as one
@@ -499,6 +555,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             if (!ok) break;
         }
         // every issued copy must land before the CTA may exit
+        cp_async_wait_all();
         if (lane == 0)
             for (int s = 0; s < C::kStages; ++s)
                 if (issued_mask & (1u << s)) mbar_wait_drain(smem_u32(&full[s]), (issued_parity >> s) & 1u, args.err);
@@ -527,6 +584,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 const uint32_t b_kb_bytes = kActBoxHeights[act_box_index(I.n)] * kKBytes;
                 for (int kb = kb0; kb < kb1; kb += C::kKPS) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) { ok = false; break; }
+                    // gathered rows were written by cp.async (generic proxy): order them
+                    // before the MMAs' reads
+                    if (KIND == Kind::GateUp && args.gather_rows) fence_proxy_async_smem();
                     const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
 #pragma unroll
                     for (int h = 0; h < C::kKPS; ++h) {

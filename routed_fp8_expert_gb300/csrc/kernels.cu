@@ -32,7 +32,7 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
                            int32_t *offsets, int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b,
                            int32_t *counters, int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm,
                            float *sx_perm, int *launches,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool copy_rows) {
     const int C = (T + 31) / 32;
     const size_t smem = sizeof(uint32_t) * kPermWarps * E;
     unsigned int *err = nullptr;
@@ -48,7 +48,7 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
     if (e != cudaSuccess) return e;
     const int threads = min(1024, max(64, d / 16));
     e = launch_pdl(perm_scatter_kernel, dim3(T), dim3(threads), 0, stream, idx, rank, cnt, offsets, xq, sx, T, k, S,
-                   E, d, C, sorted_tok, inv_pos, xq_perm, sx_perm, err);
+                   E, d, C, sorted_tok, inv_pos, xq_perm, sx_perm, err, copy_rows ? 1 : 0);
     *launches += 4;
     return e;
 }

@@ -370,15 +370,16 @@ __global__ void sched_kernel(const int32_t *__restrict__ offsets, int E, int S, 
     schedule_block(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a, tile_prefix_b, counters);
 }
 
-// One block per token: writes sorted_tok / inv_pos and copies the token's
-// quantised row and scales to its k routed positions and its S shared rows.
+// One block per token: writes sorted_tok / inv_pos and, when copy_rows, copies the
+// token's quantised row and scales to its k routed positions and its S shared rows
+// (a caller whose GEMM gathers the rows by sorted_tok skips the copy).
 // sx is row-major [T, d/128]; sx_perm is K-block-major [d/128, R].
 __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ rank,
                                     const int32_t *__restrict__ cnt_scan, const int32_t *__restrict__ offsets,
                                     const uint8_t *__restrict__ xq, const float *__restrict__ sx, int T, int k,
                                     int S, int E, int d, int C, int32_t *__restrict__ sorted_tok,
                                     int32_t *__restrict__ inv_pos, uint8_t *__restrict__ xq_perm,
-                                    float *__restrict__ sx_perm, unsigned int *err) {
+                                    float *__restrict__ sx_perm, unsigned int *err, int copy_rows) {
     pdl_trigger();
     pdl_wait();
     __shared__ int32_t s_pos[40];
@@ -403,6 +404,7 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
     } else if (threadIdx.x < ndst) {
         s_pos[threadIdx.x] = k * T + (threadIdx.x - k) * T + t;
     }
+    if (!copy_rows) return;   // uniform over the block
     __syncthreads();
     const uint4 *src = reinterpret_cast<const uint4 *>(xq + static_cast<size_t>(t) * d);
     const int nvec = d / 16;

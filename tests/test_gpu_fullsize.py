@@ -69,8 +69,12 @@ def _check_workload(shape, ex, seed, pin_layer=False):
     offsets, sorted_tok, inv_pos, xq_perm, sx_perm = moe.permute(idx, xq, sx, cfg)
     o = moe.expert_gemm_fp8(xq_perm, sx_perm, offsets, ex, cfg, T)
     y = moe.layer_forward(xd, wgd, bd, ex, cfg)
+    y_chain = moe.combine(o, w, inv_pos, cfg, T)
     torch.cuda.synchronize()
     moe.check_device_error(DEV)
+    # the one-call layer (at decode: activation rows gathered by the gate/up kernel)
+    # and the chain of separate calls (the permutation's copy) give the same bits
+    assert torch.equal(y, y_chain)
 
     # routing and permutation of all tokens
     xf = x.float().numpy()

@@ -58,3 +58,23 @@ def test_y_buffer_reuse_and_repeatability():
     y2 = moe.layer_forward(inp.x.to(DEV), inp.w_gate.to(DEV), inp.bias.to(DEV), ex, cfg, ws=ws)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2), "the layer is deterministic"
+
+
+@pytest.mark.parametrize("shape", [S.MoEShape("gather_t31", T=31, d=1024, E=32, topk=8, H=256),
+                                   S.MoEShape("gather_t48_s2", T=48, d=512, E=32, topk=8, H=384, n_shared=2),
+                                   S.MoEShape("gather_t1", T=1, d=256, E=16, topk=4, H=128)])
+def test_decode_layer_gathers_rows_like_the_permuted_copy(shape):
+    # in the decode regime moe_layer_forward's gate/up kernel gathers each token's
+    # codes and scales by sorted_tok instead of reading the permutation's copy: the
+    # output must equal the chain of separate calls (which uses the copy) bit for bit
+    inp = S.gen_moe_inputs(shape, seed=shape.T + 7, device=DEV)
+    cfg = moe.cfg_of(shape)
+    y = moe.layer_forward(inp.x, inp.w_gate, inp.bias, inp.experts, cfg)
+    idx, w, _ = moe.route(inp.x, inp.w_gate, inp.bias, cfg)
+    xq, sx = moe.quant_fp8_1x128(inp.x)
+    offs, st, inv, xqp, sxp = moe.permute(idx, xq, sx, cfg)
+    o = moe.expert_gemm_fp8(xqp, sxp, offs, inp.experts, cfg, shape.T)
+    y_chain = moe.combine(o, w, inv, cfg, shape.T)
+    torch.cuda.synchronize()
+    moe.check_device_error(DEV)
+    assert torch.equal(y, y_chain)
