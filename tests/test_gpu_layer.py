@@ -61,12 +61,16 @@ def test_y_buffer_reuse_and_repeatability():
 
 
 @pytest.mark.parametrize("shape", [S.MoEShape("gather_t31", T=31, d=1024, E=32, topk=8, H=256),
+                                   S.MoEShape("gather_wide_t200", T=200, d=1024, E=32, topk=8, H=256),
+                                   S.MoEShape("gather_wide_t480_s2", T=480, d=512, E=32, topk=8, H=384, n_shared=2),
                                    S.MoEShape("gather_t48_s2", T=48, d=512, E=32, topk=8, H=384, n_shared=2),
                                    S.MoEShape("gather_t1", T=1, d=256, E=16, topk=4, H=128)])
-def test_decode_layer_gathers_rows_like_the_permuted_copy(shape):
+def test_one_call_layer_equals_the_separate_calls(shape):
     # in the decode regime moe_layer_forward's gate/up kernel gathers each token's
-    # codes and scales by sorted_tok instead of reading the permutation's copy: the
-    # output must equal the chain of separate calls (which uses the copy) bit for bit
+    # codes and scales by sorted_tok instead of reading the permutation's copy; beyond
+    # it (T = 200 and 480 here, with some experts on a second, ragged tile) the one
+    # call runs the token-major kernels on the copy. Either way the output must equal
+    # the chain of separate calls bit for bit
     inp = S.gen_moe_inputs(shape, seed=shape.T + 7, device=DEV)
     cfg = moe.cfg_of(shape)
     y = moe.layer_forward(inp.x, inp.w_gate, inp.bias, inp.experts, cfg)
