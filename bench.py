@@ -396,8 +396,6 @@ def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
     # persistent buffers of the step
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     w = torch.empty((T, k), dtype=torch.float32, device=dev)
-    xq = torch.empty((T, d), dtype=torch.uint8, device=dev)
-    sx = torch.empty((T, d // 128), dtype=torch.float32, device=dev)
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     sorted_tok = torch.empty(T * k, dtype=torch.int32, device=dev)
     inv_pos = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -419,7 +417,7 @@ def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
             raise RuntimeError(L.moe_last_error_string().decode())
         return L.moe_last_launch_count()
 
-    names = ["route", "quant", "permute", "gateup", "down", "combine"]
+    names = ["route", "quant_permute", "gateup", "down", "combine"]
 
     def step(ev=None):
         n = 0
@@ -428,31 +426,28 @@ def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
         n += call(L.moe_route(P(x), P(wg), P(b), cref, T, P(idx), P(w), None, P(ws), nws, st))
         if ev is not None:
             ev[1].record()
-        n += call(L.moe_quant_fp8_1x128(P(x), 1, T, d, P(xq), P(sx), 0, st))
+        n += call(L.moe_quant_permute_fp8(P(idx), P(x), cref, T, P(offsets), P(sorted_tok), P(inv_pos),
+                                          P(xq_perm), P(sx_perm), P(ws), nws, st))
         if ev is not None:
             ev[2].record()
-        n += call(L.moe_permute(P(idx), P(xq), P(sx), cref, T, P(offsets), P(sorted_tok), P(inv_pos), P(xq_perm),
-                                P(sx_perm), P(ws), nws, st))
-        if ev is not None:
-            ev[3].record()
         n += call(L.moe_expert_gateup_fp8(P(xq_perm), P(sx_perm), P(offsets), P(ex.w13), P(ex.w13_s), cref, T,
                                           P(hq), P(hs), P(ws), nws, st))
         if ev is not None:
-            ev[4].record()
+            ev[3].record()
         n += call(L.moe_expert_down_fp8(P(hq), P(hs), P(offsets), P(ex.w2), P(ex.w2_s), cref, T, P(o), P(ws), nws,
                                         st))
         if ev is not None:
-            ev[5].record()
+            ev[4].record()
         n += call(L.moe_combine(P(o), P(w), P(inv_pos), cref, T, P(y), st))
         if ev is not None:
-            ev[6].record()
+            ev[5].record()
         return n
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     moe.check_device_error(dev)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev.index or 0)

@@ -116,6 +116,18 @@ int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx,
                 uint8_t *xq_perm, float *sx_perm,
                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* moe_quant_fp8_1x128 of x (in_is_bf16 = 1, s_transposed = 0) followed by
+ * moe_permute, in one pass over x: each token's 1x128 codes and scales are
+ * computed once and written straight to its permuted rows, and the unpermuted
+ * codes are never stored.
+ * x [T, d] bf16; every other argument and output as moe_permute's. The outputs
+ * equal those of the two calls bit for bit. Pointers 16-byte aligned. */
+int moe_quant_permute_fp8(const int32_t *topk_idx, const void *x,
+                          const moe_cfg_t *cfg, int T,
+                          int32_t *offsets, int32_t *sorted_tok, int32_t *inv_pos,
+                          uint8_t *xq_perm, float *sx_perm,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
 /* moe_permute without a caller workspace. The pages have no counterpart: this
  * entry point exists for callers that cannot provide scratch memory, such as a
  * plugin inside a host application that owns every device allocation, or a

@@ -33,6 +33,8 @@ _SIGS = {
     "moe_route": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_permute": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                              _c_size, _vp]),
+    "moe_quant_permute_fp8": (_c_int, [_vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _c_size, _vp]),
     "moe_permute_noalloc": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _vp,
                                      _vp]),
     "moe_expert_gemm_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp,
@@ -158,6 +160,26 @@ def permute(topk_idx, xq, sx, cfg: MoeCfg, ws=None):
     ws = workspace(cfg, T, dev) if ws is None else ws
     _check(load().moe_permute(_p(topk_idx), _p(xq), _p(sx), ctypes.byref(cfg), T, _p(offsets), _p(sorted_tok),
                               _p(inv_pos), _p(xq_perm), _p(sx_perm), _p(ws), ws.numel(), _stream(dev)))
+    return offsets, sorted_tok, inv_pos, xq_perm, sx_perm
+
+
+def quant_permute_fp8(topk_idx, x, cfg: MoeCfg, ws=None):
+    """moe_quant_permute_fp8: the 1x128 codes of bf16 x written straight to their
+    permuted rows. Outputs as permute() of quant_fp8_1x128(x)."""
+    _cuda(topk_idx, x)
+    if x.dtype != torch.bfloat16:
+        raise MoeError(MOE_ERR_ARG, "x must be bf16")
+    T = topk_idx.shape[0]
+    dev = topk_idx.device
+    R = permuted_rows(cfg, T)
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    sorted_tok = torch.empty(T * cfg.topk, dtype=torch.int32, device=dev)
+    inv_pos = torch.empty((T, cfg.topk), dtype=torch.int32, device=dev)
+    xq_perm = torch.empty((R, cfg.d), dtype=torch.uint8, device=dev)
+    sx_perm = torch.empty((cfg.d // 128, R), dtype=torch.float32, device=dev)
+    ws = workspace(cfg, T, dev) if ws is None else ws
+    _check(load().moe_quant_permute_fp8(_p(topk_idx), _p(x), ctypes.byref(cfg), T, _p(offsets), _p(sorted_tok),
+                                        _p(inv_pos), _p(xq_perm), _p(sx_perm), _p(ws), ws.numel(), _stream(dev)))
     return offsets, sorted_tok, inv_pos, xq_perm, sx_perm
 
 

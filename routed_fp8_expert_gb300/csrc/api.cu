@@ -511,6 +511,33 @@ int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx, con
     return MOE_OK;
 }
 
+int moe_quant_permute_fp8(const int32_t *topk_idx, const void *x, const moe_cfg_t *cfg, int T, int32_t *offsets,
+                          int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm, float *sx_perm, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    t_launches = 0;
+    MOE_CHECK(check_cfg(cfg));
+    MOE_CHECK(check_T(T));
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(topk_idx, "topk_idx"));
+    MOE_CHECK(check_ptr(x, "x"));
+    MOE_CHECK(check_ptr(offsets, "offsets"));
+    MOE_CHECK(check_ptr(sorted_tok, "sorted_tok"));
+    MOE_CHECK(check_ptr(inv_pos, "inv_pos"));
+    MOE_CHECK(check_ptr(xq_perm, "xq_perm"));
+    MOE_CHECK(check_ptr(sx_perm, "sx_perm"));
+    const LayerWs need = carve_layer(*cfg, T, nullptr);
+    MOE_CHECK(check_ws(workspace, workspace_bytes, need.bytes));
+    const LayerWs ws = carve_layer(*cfg, T, workspace);
+    int n = 0;
+    MOE_CUDA(launch_permute(topk_idx, nullptr, nullptr, T, cfg->topk, cfg->n_shared, cfg->E, cfg->d,
+                            expert_bn(*cfg, T), down_bn(*cfg, T), ws.rank, ws.cnt, ws.counts, offsets, ws.row_start,
+                            ws.tile_prefix, ws.tile_prefix_dn, ws.counters, sorted_tok, inv_pos, xq_perm, sx_perm, &n,
+                            static_cast<cudaStream_t>(stream), true, x),
+             "quantise + permutation launch");
+    t_launches = n;
+    return MOE_OK;
+}
+
 int moe_expert_gemm_fp8(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets, const uint8_t *w13,
                         const float *w13_s, const uint8_t *w2, const float *w2_s, const moe_cfg_t *cfg, int T,
                         void *o, void *workspace, size_t workspace_bytes, void *stream) {
@@ -663,17 +690,17 @@ int moe_layer_forward(const void *x, const void *w_gate, const float *bias, cons
     int n = 0;
     MOE_CHECK(route_impl(x, w_gate, bias, c, T, idx, w, nullptr, ws.logits, st));
     n += t_launches;
-    MOE_CUDA(launch_quant(x, true, T, c.d, ws.xq, ws.sx, false, num_sms(), st), "quantise launch");
-    n += 1;
-    // decode regime: the gate/up kernel gathers the activation rows by sorted_tok,
-    // so the permutation writes no copy of them
+    // the permutation quantises x on the way (one pass over x). Decode regime: the
+    // gate/up kernel gathers the activation rows by sorted_tok, so the permutation
+    // writes the unpermuted codes and no permuted copy
     const bool gather = decode_regime(c, T);
     const Gather g{ws.xq, ws.sx, ws.sorted_tok};
     int np = 0;
-    MOE_CUDA(launch_permute(idx, ws.xq, ws.sx, T, c.topk, c.n_shared, c.E, c.d, expert_bn(c, T), down_bn(c, T),
+    MOE_CUDA(launch_permute(idx, nullptr, nullptr, T, c.topk, c.n_shared, c.E, c.d, expert_bn(c, T), down_bn(c, T),
                             ws.rank, ws.cnt, ws.counts, ws.offsets, ws.row_start, ws.tile_prefix, ws.tile_prefix_dn,
-                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st, !gather),
-             "permutation launch");
+                            ws.counters, ws.sorted_tok, ws.inv_pos, ws.xq_perm, ws.sx_perm, &np, st, !gather, x,
+                            gather ? ws.xq : nullptr, gather ? ws.sx : nullptr),
+             "quantise + permutation launch");
     n += np;
     t_launches = 0;
     // the permutation already wrote the GEMM schedule into the workspace

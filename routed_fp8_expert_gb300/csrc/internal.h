@@ -54,7 +54,8 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
                            int32_t *offsets, int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b,
                            int32_t *counters, int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm,
                            float *sx_perm, int *launches,
-                           cudaStream_t stream, bool copy_rows = true);
+                           cudaStream_t stream, bool copy_rows = true, const void *x_bf16 = nullptr,
+                           uint8_t *xq_out = nullptr, float *sx_out = nullptr);
 cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
                          int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b, int32_t *counters,
                          cudaStream_t stream);

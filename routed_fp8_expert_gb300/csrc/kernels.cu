@@ -8,8 +8,8 @@ namespace moe {
 cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint8_t *q, float *s,
                          bool s_transposed, int num_sms, cudaStream_t stream) {
     const int64_t groups = rows * (cols / 128);
-    const int threads = 256;
-    int64_t blocks = (groups + 7) / 8;
+    const int threads = 256;   // eight warps, each with 2 * kQuantPairs groups per trip
+    int64_t blocks = (groups + 8 * 2 * kQuantPairs - 1) / (8 * 2 * kQuantPairs);
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     const int st = s_transposed ? 1 : 0;
@@ -23,8 +23,22 @@ cudaError_t launch_quant(const void *in, bool bf16, int64_t rows, int cols, uint
 cudaError_t launch_topk(const float *logits, int splits, const float *bias, int T, int E, int k, float scale,
                         int32_t *idx, float *w, float *scores, cudaStream_t stream) {
     const int threads = 64;   // 2 tokens per block: a 256-token batch spreads over 128 blocks
-    return launch_pdl(topk_kernel, dim3((T + 1) / 2), dim3(threads), 0, stream, logits, splits, bias, T, E, k, scale,
-                      idx, w, scores);
+    const dim3 grid((T + 1) / 2);
+    const int nper = (E + 31) / 32;   // E <= 1024
+    if (nper <= 4)
+        return launch_pdl(topk_kernel<4>, grid, dim3(threads), 0, stream, logits, splits, bias, T, E, k, scale, idx, w,
+                          scores);
+    if (nper <= 8)
+        return launch_pdl(topk_kernel<8>, grid, dim3(threads), 0, stream, logits, splits, bias, T, E, k, scale, idx, w,
+                          scores);
+    if (nper <= 12)
+        return launch_pdl(topk_kernel<12>, grid, dim3(threads), 0, stream, logits, splits, bias, T, E, k, scale, idx, w,
+                          scores);
+    if (nper <= 16)
+        return launch_pdl(topk_kernel<16>, grid, dim3(threads), 0, stream, logits, splits, bias, T, E, k, scale, idx, w,
+                          scores);
+    return launch_pdl(topk_kernel<32>, grid, dim3(threads), 0, stream, logits, splits, bias, T, E, k, scale, idx, w,
+                      scores);
 }
 
 cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *sx, int T, int k, int S, int E,
@@ -32,7 +46,8 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
                            int32_t *offsets, int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b,
                            int32_t *counters, int32_t *sorted_tok, int32_t *inv_pos, uint8_t *xq_perm,
                            float *sx_perm, int *launches,
-                           cudaStream_t stream, bool copy_rows) {
+                           cudaStream_t stream, bool copy_rows, const void *x_bf16, uint8_t *xq_out,
+                           float *sx_out) {
     const int C = (T + 31) / 32;
     const size_t smem = sizeof(uint32_t) * kPermWarps * E;
     unsigned int *err = nullptr;
@@ -46,9 +61,18 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
     e = launch_pdl(perm_offsets_kernel, dim3(1), dim3(1024), 0, stream, counts, E, S, T, k, tile_a, tile_b, offsets,
                    row_start, tile_prefix_a, tile_prefix_b, counters);
     if (e != cudaSuccess) return e;
-    const int threads = min(1024, max(64, d / 16));
-    e = launch_pdl(perm_scatter_kernel, dim3(T), dim3(threads), 0, stream, idx, rank, cnt, offsets, xq, sx, T, k, S,
-                   E, d, C, sorted_tok, inv_pos, xq_perm, sx_perm, err, copy_rows ? 1 : 0);
+    if (x_bf16) {
+        // kScatterUnits 8-element units per thread: 224 threads at d = 7168
+        const int per = (d / 8 + kScatterUnits - 1) / kScatterUnits;
+        const int threads = (min(1024, max(64, per)) + 31) / 32 * 32;
+        e = launch_pdl(perm_quant_scatter_kernel, dim3(T), dim3(threads), 0, stream, idx, rank, cnt, offsets,
+                       static_cast<const __nv_bfloat16 *>(x_bf16), T, k, S, E, d, C, sorted_tok, inv_pos, xq_perm,
+                       sx_perm, copy_rows ? 1 : 0, xq_out, sx_out, err);
+    } else {
+        const int threads = min(1024, max(64, d / 16));
+        e = launch_pdl(perm_scatter_kernel, dim3(T), dim3(threads), 0, stream, idx, rank, cnt, offsets, xq, sx, T, k,
+                       S, E, d, C, sorted_tok, inv_pos, xq_perm, sx_perm, err, copy_rows ? 1 : 0);
+    }
     *launches += 4;
     return e;
 }

@@ -45,77 +45,94 @@ __device__ __forceinline__ void div_by_scale(const float (&x)[N], float s, float
     }
 }
 
-// One warp per 128-wide group: lane l holds elements 4l..4l+3.
+// Half a warp per 128-wide group (lane l of the half holds elements 8l..8l+7, one
+// 16-byte load of bf16), two groups per warp and kQuantPairs pairs per loop trip, so
+// each warp has four groups' loads in flight. Groups are numbered row-major (group g
+// of row r is r * cols/128 + g); trip j of warp w takes the pairs of groups
+// 2 (w + (j * kQuantPairs + u) * nwarps) + half, u < kQuantPairs.
 // s = amax / 448 (IEEE fp32 division), q = e4m3(x / s) (x / s correctly rounded,
 // RNE to e4m3, saturating); amax = 0 gives s = 0 and zero codes.
+constexpr int kQuantPairs = 2;
+
 template <bool kBf16In>
 __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, int cols,
                                    uint8_t *__restrict__ q, float *__restrict__ s, int s_transposed) {
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
+    const int half = lane >> 4, l16 = lane & 15;
     const int gpr = cols / 128;
     const int64_t n_groups = rows * gpr;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    // (row, group) of the warp's group, advanced by the grid stride without a
-    // division per group (a 64-bit division is a long instruction sequence; the
-    // two here are 32-bit whenever the counts fit)
-    int64_t r, dr;
-    int g, dg;
-    if (n_groups <= 0x7fffffff) {
-        const uint32_t w0 = static_cast<uint32_t>(warp0), nw = static_cast<uint32_t>(nwarps);
-        const uint32_t ug = static_cast<uint32_t>(gpr);
-        r = w0 / ug;
-        g = static_cast<int>(w0 - static_cast<uint32_t>(r) * ug);
-        dr = nw / ug;
-        dg = static_cast<int>(nw - static_cast<uint32_t>(dr) * ug);
-    } else {
-        r = warp0 / gpr;
-        g = static_cast<int>(warp0 - r * gpr);
-        dr = nwarps / gpr;
-        dg = static_cast<int>(nwarps - dr * gpr);
-    }
-    for (int64_t gi = warp0; gi < n_groups; gi += nwarps) {
-        const int64_t base = r * cols + g * 128 + lane * 4;
-        float v[4];
-        if constexpr (kBf16In) {
-            const uint2 raw = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(in) + base);
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-            v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
+    // (row, group) of group index gi; a 64-bit division is a long instruction
+    // sequence, so the 32-bit one whenever the count fits
+    const bool narrow = n_groups <= 0x7fffffff;
+    auto split = [&](int64_t gi, int64_t &r, int &g) {
+        if (narrow) {
+            const uint32_t ur = static_cast<uint32_t>(gi) / static_cast<uint32_t>(gpr);
+            r = ur;
+            g = static_cast<int>(static_cast<uint32_t>(gi) - ur * static_cast<uint32_t>(gpr));
         } else {
-            const float4 f = *reinterpret_cast<const float4 *>(static_cast<const float *>(in) + base);
-            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+            r = gi / gpr;
+            g = static_cast<int>(gi - r * gpr);
         }
-        unsigned m = 0;
+    };
+    for (int64_t p0 = warp0; 2 * p0 < n_groups; p0 += kQuantPairs * nwarps) {
+        float v[kQuantPairs][8];
+        int64_t base[kQuantPairs], gi[kQuantPairs], rr[kQuantPairs];
+        int gg[kQuantPairs];
+        // all the loads first
 #pragma unroll
-        for (int i = 0; i < 4; ++i) m = max(m, __float_as_uint(fabsf(v[i])));
-        const float amax = __uint_as_float(__reduce_max_sync(kFull, m));
-        const float sc = amax / 448.0f;
-        uint32_t packed = 0;
-        if (amax != 0.f) {
-            float d4[4];
-            div_by_scale(v, sc, d4);
-            const uint32_t lo = e4m3x2(d4[0], d4[1]);
-            const uint32_t hi = e4m3x2(d4[2], d4[3]);
-            packed = lo | (hi << 16);
+        for (int u = 0; u < kQuantPairs; ++u) {
+            gi[u] = 2 * (p0 + u * nwarps) + half;
+            split(gi[u] < n_groups ? gi[u] : 0, rr[u], gg[u]);
+            base[u] = rr[u] * cols + gg[u] * 128 + l16 * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
+            if (gi[u] < n_groups) {
+                if constexpr (kBf16In) {
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(in) + base[u]), v[u]);
+                } else {
+                    const float4 a = *reinterpret_cast<const float4 *>(static_cast<const float *>(in) + base[u]);
+                    const float4 b = *reinterpret_cast<const float4 *>(static_cast<const float *>(in) + base[u] + 4);
+                    v[u][0] = a.x; v[u][1] = a.y; v[u][2] = a.z; v[u][3] = a.w;
+                    v[u][4] = b.x; v[u][5] = b.y; v[u][6] = b.z; v[u][7] = b.w;
+                }
+            }
         }
-        *reinterpret_cast<uint32_t *>(q + base) = packed;
-        if (lane == 0) s[s_transposed ? (static_cast<int64_t>(g) * rows + r) : (r * gpr + g)] = sc;
-        r += dr;
-        g += dg;
-        if (g >= gpr) {
-            g -= gpr;
-            ++r;
+#pragma unroll
+        for (int u = 0; u < kQuantPairs; ++u) {
+            unsigned m = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = max(m, __float_as_uint(fabsf(v[u][i])));
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off, 16));
+            if (gi[u] >= n_groups) continue;
+            const float amax = __uint_as_float(m);
+            const float sc = amax / 448.0f;
+            uint2 packed = make_uint2(0u, 0u);
+            if (amax != 0.f) {
+                float d8[8];
+                div_by_scale(v[u], sc, d8);
+                packed.x = static_cast<uint32_t>(e4m3x2(d8[0], d8[1])) | (static_cast<uint32_t>(e4m3x2(d8[2], d8[3])) << 16);
+                packed.y = static_cast<uint32_t>(e4m3x2(d8[4], d8[5])) | (static_cast<uint32_t>(e4m3x2(d8[6], d8[7])) << 16);
+            }
+            *reinterpret_cast<uint2 *>(q + base[u]) = packed;
+            if (l16 == 0) s[s_transposed ? (static_cast<int64_t>(gg[u]) * rows + rr[u]) : gi[u]] = sc;
         }
     }
 }
 
 // ------------------------------------------------------------------ top-k
-// One warp per token. The logit is the sum of the router GEMM's K-split
-// partials, added in split order; scores s = sigmoid(logit) in fp32; choice
-// c = s + bias; k rounds of a warp arg-max on (c desc, expert id asc); weights from s.
+// One warp per token; lane l holds experts l + 32 i, i < NPER (NPER >= ceil(E / 32)).
+// The logit is the sum of the router GEMM's K-split partials, added in split order;
+// scores s = sigmoid(logit) in fp32; choice c = s + bias. Each lane keeps the best
+// of its own choices (c desc, expert id asc: its ids ascend with i, so the first
+// strict maximum); each of the k rounds takes the warp's best of the lanes' bests,
+// and only the lane that owned it strikes it out and rescans its own NPER values.
+// Weights come from s.
+template <int NPER>
 __global__ void topk_kernel(const float *__restrict__ logits, int splits, const float *__restrict__ bias,
                             int T, int E, int k, float route_scale, int32_t *__restrict__ topk_idx,
                             float *__restrict__ topk_w, float *__restrict__ scores) {
@@ -126,21 +143,20 @@ __global__ void topk_kernel(const float *__restrict__ logits, int splits, const 
     if (t >= T) return;
     const float *lrow = logits + static_cast<size_t>(t) * E;
     const size_t split_stride = static_cast<size_t>(T) * E;
-    float sv[32], cv[32];
-    const int nper = (E + 31) >> 5;
+    float sv[NPER], cv[NPER];
     // logits: the split partials added in split order (independent loads per split)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) sv[i] = (i < nper && lane + 32 * i < E) ? lrow[lane + 32 * i] : 0.f;
+    for (int i = 0; i < NPER; ++i) sv[i] = (lane + 32 * i < E) ? lrow[lane + 32 * i] : 0.f;
     for (int sp = 1; sp < splits; ++sp) {
         const float *prow = lrow + sp * split_stride;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < nper && lane + 32 * i < E) sv[i] += prow[lane + 32 * i];
+        for (int i = 0; i < NPER; ++i)
+            if (lane + 32 * i < E) sv[i] += prow[lane + 32 * i];
     }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
-        if (i < nper && e < E) {
+        if (e < E) {
             const float sc = 1.0f / (1.0f + expf(-sv[i]));
             sv[i] = sc;
             cv[i] = sc + bias[e];
@@ -150,15 +166,21 @@ __global__ void topk_kernel(const float *__restrict__ logits, int splits, const 
             cv[i] = -INFINITY;
         }
     }
+    float lb;   // the lane's best remaining choice and its expert id
+    int le;
+    auto rescan = [&]() {
+        lb = -INFINITY;
+        le = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i)
+            if (cv[i] > lb) { lb = cv[i]; le = lane + 32 * i; }
+    };
+    rescan();
     int my_idx = 0;
     float my_s = 0.f;
     for (int r = 0; r < k; ++r) {
-        float best = -INFINITY;
-        int best_e = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (i < nper && cv[i] > best) { best = cv[i]; best_e = lane + 32 * i; }
-        }
+        float best = lb;
+        int best_e = le;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float ob = __shfl_xor_sync(kFull, best, off);
@@ -168,9 +190,11 @@ __global__ void topk_kernel(const float *__restrict__ logits, int splits, const 
         const int owner = best_e & 31;
         const int slot = best_e >> 5;
         float mine = 0.f;
+        if (lane == owner) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (i == slot && lane == owner) { mine = sv[i]; cv[i] = -INFINITY; }
+            for (int i = 0; i < NPER; ++i)
+                if (i == slot) { mine = sv[i]; cv[i] = -INFINITY; }
+            rescan();
         }
         const float s_sel = __shfl_sync(kFull, mine, owner);
         if (lane == r) { my_idx = best_e; my_s = s_sel; }
@@ -370,6 +394,34 @@ __global__ void sched_kernel(const int32_t *__restrict__ offsets, int E, int S, 
     schedule_block(offsets, E, S, T, k, tile_a, tile_b, row_start, tile_prefix_a, tile_prefix_b, counters);
 }
 
+// Token t's destinations, by the block's first k + S threads: assignment j < k
+// goes to offsets[e] + cnt_scan[e][t / 32] + rank[t, j] (written to inv_pos, and t
+// to sorted_tok there; an id outside [0, E) or a position outside [0, kT) gives -1
+// and no write), shared expert s to row kT + sT + t. s_pos[j] holds them.
+__device__ __forceinline__ void scatter_positions(const int32_t *__restrict__ idx, const int32_t *__restrict__ rank,
+                                                  const int32_t *__restrict__ cnt_scan,
+                                                  const int32_t *__restrict__ offsets, int t, int T, int k, int S,
+                                                  int E, int C, int32_t *__restrict__ sorted_tok,
+                                                  int32_t *__restrict__ inv_pos, int32_t *s_pos, unsigned int *err) {
+    if (threadIdx.x < k) {
+        const int j = threadIdx.x;
+        const int e = idx[static_cast<size_t>(t) * k + j];
+        int pos = -1;
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+            pos = offsets[e] + cnt_scan[static_cast<size_t>(e) * C + (t >> 5)] + rank[static_cast<size_t>(t) * k + j];
+            if (pos < 0 || pos >= k * T) {
+                if (kDebugBounds) record_error(err, ERR_BAD_INDEX);
+                pos = -1;
+            }
+        }
+        s_pos[j] = pos;
+        inv_pos[static_cast<size_t>(t) * k + j] = pos;
+        if (pos >= 0) sorted_tok[pos] = t;
+    } else if (threadIdx.x < k + S) {
+        s_pos[threadIdx.x] = k * T + (threadIdx.x - k) * T + t;
+    }
+}
+
 // One block per token: writes sorted_tok / inv_pos and, when copy_rows, copies the
 // token's quantised row and scales to its k routed positions and its S shared rows
 // (a caller whose GEMM gathers the rows by sorted_tok skips the copy).
@@ -384,26 +436,9 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
     pdl_wait();
     __shared__ int32_t s_pos[40];
     const int t = blockIdx.x;
-    const int c = t >> 5;
     const int64_t R = static_cast<int64_t>(k + S) * T;
     const int ndst = k + S;
-    if (threadIdx.x < k) {
-        const int j = threadIdx.x;
-        const int e = idx[static_cast<size_t>(t) * k + j];
-        int pos = -1;
-        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
-            pos = offsets[e] + cnt_scan[static_cast<size_t>(e) * C + c] + rank[static_cast<size_t>(t) * k + j];
-            if (pos < 0 || pos >= k * T) {
-                if (kDebugBounds) record_error(err, ERR_BAD_INDEX);
-                pos = -1;
-            }
-        }
-        s_pos[j] = pos;
-        inv_pos[static_cast<size_t>(t) * k + j] = pos;
-        if (pos >= 0) sorted_tok[pos] = t;
-    } else if (threadIdx.x < ndst) {
-        s_pos[threadIdx.x] = k * T + (threadIdx.x - k) * T + t;
-    }
+    scatter_positions(idx, rank, cnt_scan, offsets, t, T, k, S, E, C, sorted_tok, inv_pos, s_pos, err);
     if (!copy_rows) return;   // uniform over the block
     __syncthreads();
     const uint4 *src = reinterpret_cast<const uint4 *>(xq + static_cast<size_t>(t) * d);
@@ -418,6 +453,80 @@ __global__ void perm_scatter_kernel(const int32_t *__restrict__ idx, const int32
         const float sc = sx[static_cast<size_t>(t) * gpr + g];
         for (int j = 0; j < ndst; ++j)
             if (s_pos[j] >= 0) sx_perm[static_cast<size_t>(g) * R + s_pos[j]] = sc;
+    }
+}
+
+// perm_scatter_kernel with the 1x128 quantisation of the bf16 row on the way, in
+// quant_1x128_kernel's arithmetic: one block per token; thread i holds the 8-element
+// units u = i + blockDim * n of the row (elements 8u..8u+7), kScatterUnits of them
+// loaded together. A 128-wide group is 16
+// consecutive units, held by a half-warp (blockDim a multiple of 32, d a multiple
+// of 128). Codes and scale go to the token's k routed positions and S shared rows
+// when copy_rows, and to the unpermuted xq_out [T, d] / sx_out [T, d/128]
+// (row-major) when xq_out is given.
+constexpr int kScatterUnits = 4;
+
+__global__ void perm_quant_scatter_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ rank,
+                                          const int32_t *__restrict__ cnt_scan, const int32_t *__restrict__ offsets,
+                                          const __nv_bfloat16 *__restrict__ x, int T, int k, int S, int E, int d,
+                                          int C, int32_t *__restrict__ sorted_tok, int32_t *__restrict__ inv_pos,
+                                          uint8_t *__restrict__ xq_perm, float *__restrict__ sx_perm, int copy_rows,
+                                          uint8_t *__restrict__ xq_out, float *__restrict__ sx_out,
+                                          unsigned int *err) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int32_t s_pos[40];
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const unsigned half_mask = 0xffffu << (lane & 16);
+    const int64_t R = static_cast<int64_t>(k + S) * T;
+    const int ndst = copy_rows ? k + S : 0;
+    const int nunits = d / 8;
+    const int gpr = d / 128;
+    const int nthr = static_cast<int>(blockDim.x);
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * d);
+    uint4 raw[kScatterUnits];
+    auto load_batch = [&](int base) {
+#pragma unroll
+        for (int i = 0; i < kScatterUnits; ++i) {
+            const int u = base + static_cast<int>(threadIdx.x) + i * nthr;
+            raw[i] = u < nunits ? xr[u] : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    scatter_positions(idx, rank, cnt_scan, offsets, t, T, k, S, E, C, sorted_tok, inv_pos, s_pos, err);
+    __syncthreads();
+    for (int base = 0; base < nunits; base += kScatterUnits * nthr) {
+        load_batch(base);
+#pragma unroll
+        for (int i = 0; i < kScatterUnits; ++i) {
+            const int u = base + static_cast<int>(threadIdx.x) + i * nthr;
+            if (u >= nunits) continue;   // whole half-warps: nunits and nthr are multiples of 16
+            float v[8];
+            unpack_bf16x8(raw[i], v);
+            unsigned m = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) m = max(m, __float_as_uint(fabsf(v[q])));
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(half_mask, m, off, 16));
+            const float amax = __uint_as_float(m);
+            const float sc = amax / 448.0f;
+            uint2 codes = make_uint2(0u, 0u);
+            if (amax != 0.f) {
+                float d8[8];
+                div_by_scale(v, sc, d8);
+                codes.x = static_cast<uint32_t>(e4m3x2(d8[0], d8[1])) | (static_cast<uint32_t>(e4m3x2(d8[2], d8[3])) << 16);
+                codes.y = static_cast<uint32_t>(e4m3x2(d8[4], d8[5])) | (static_cast<uint32_t>(e4m3x2(d8[6], d8[7])) << 16);
+            }
+            for (int j = 0; j < ndst; ++j)
+                if (s_pos[j] >= 0) reinterpret_cast<uint2 *>(xq_perm + static_cast<size_t>(s_pos[j]) * d)[u] = codes;
+            if (xq_out) reinterpret_cast<uint2 *>(xq_out + static_cast<size_t>(t) * d)[u] = codes;
+            if ((lane & 15) == 0) {
+                const int g = u >> 4;
+                for (int j = 0; j < ndst; ++j)
+                    if (s_pos[j] >= 0) sx_perm[static_cast<size_t>(g) * R + s_pos[j]] = sc;
+                if (sx_out) sx_out[static_cast<size_t>(t) * gpr + g] = sc;
+            }
+        }
     }
 }
 

@@ -59,3 +59,36 @@ def test_skewed_counts():
         rest = rng.choice(np.setdiff1d(np.arange(E), h), 2, replace=False)
         idx[t] = np.concatenate([h, rest])
     _check(idx, E, d=128)
+
+
+def _check_quant_permute(idx, E, d, S, seed):
+    """moe_quant_permute_fp8 on bf16 x: bit for bit the permutation of the
+    quantiser's codes, and the oracle's codes of x in the oracle's row order."""
+    T, k = idx.shape
+    cfg = moe.MoeCfg(d, E, k, 128, S, 2.827)
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(T, d, generator=g) * torch.rand(T, 1, generator=g) * 10).to(torch.bfloat16)
+    if T > 2:
+        x[1, :128] = 0   # a group with amax = 0
+    ti = torch.from_numpy(idx).to(DEV)
+    xd = x.to(DEV)
+    xq, sx = moe.quant_fp8_1x128(xd)
+    ref = moe.permute(ti, xq, sx, cfg)
+    got = moe.quant_permute_fp8(ti, xd, cfg)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("offsets", "sorted_tok", "inv_pos", "xq_perm", "sx_perm"), ref, got):
+        assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                           b.view(torch.int32) if b.dtype == torch.float32 else b), name
+    qo, so = O.quantize_1x128(x.float().numpy())
+    p = O.permute(idx, E)
+    rows = np.concatenate([p["sorted_tok"]] + [np.arange(T)] * S)
+    np.testing.assert_array_equal(got[3].cpu().numpy(), qo[rows])
+    np.testing.assert_array_equal(got[4].cpu().numpy().view(np.int32), so[rows].T.view(np.int32))
+
+
+@pytest.mark.parametrize("T,E,k,d,S", [(1, 32, 8, 256, 1), (33, 32, 8, 384, 1), (70, 32, 8, 1024, 0),
+                                       (70, 32, 8, 1024, 2), (50, 64, 32, 128, 1), (257, 384, 8, 7168, 1),
+                                       (31, 40, 1, 16384, 4), (1000, 384, 8, 7168, 1)])
+def test_quant_permute_equals_quant_then_permute(T, E, k, d, S):
+    _check_quant_permute(_random_idx(T, E, k, np.random.default_rng(T + E + k + d)), E, d, S, seed=T + d)
+
