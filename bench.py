@@ -571,8 +571,9 @@ def time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks, n=50):
 def time_block_call(moe, x, wg, b, ex, cfg, ws, dev, n=20):
     """The FFN half of the block in one call (RMSNorm_post with the fused
     quantisation, the layer, residual addition and RMSNorm_next) against the
-    one-call layer on the same inputs (x as the residual stream): CUDA events, n
-    calls each after three warm-up calls."""
+    one-call layer on the same inputs (x as the residual stream), and the one-call
+    layer captured in a CUDA graph and replayed: CUDA events, n calls each after
+    three warm-up calls."""
     g_post = S.gen_norm_weight(x.shape[1], seed=1, name="norm_post", device=dev)
     g_next = S.gen_norm_weight(x.shape[1], seed=1, name="norm_next", device=dev)
     h_out = torch.empty_like(x)
@@ -594,6 +595,26 @@ def time_block_call(moe, x, wg, b, ex, cfg, ws, dev, n=20):
         torch.cuda.synchronize(dev)
         out[name] = e0.elapsed_time(e1) / n
     out["extra_ms"] = out["block_ms"] - out["layer_ms"]
+    # the one-call layer captured once in a CUDA graph and replayed (same inputs)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        calls["layer_ms"]()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls["layer_ms"]()
+    for _ in range(3):
+        graph.replay()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    out["layer_graph_ms"] = e0.elapsed_time(e1) / n
     return out
 
 
