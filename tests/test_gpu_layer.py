@@ -38,6 +38,15 @@ def test_toy_layer(T):
     _layer(shape, seed=T)
 
 
+# several shared experts in the token-major regime (each a group of T rows after the
+# routed segments), and one-tile routed experts (T = 100: 25 rows each on average)
+# next to experts of a ragged second tile (T = 388: 97 on average)
+@pytest.mark.parametrize("T,n_shared", [(100, 2), (100, 4), (388, 1)])
+def test_toy_layer_shared_experts(T, n_shared):
+    shape = S.MoEShape(f"toy_shared_t{T}_s{n_shared}", T=T, d=1024, E=32, topk=8, H=256, n_shared=n_shared)
+    _layer(shape, seed=T + n_shared)
+
+
 def test_toy_layer_reference_workload():
     _layer(S.TOY, seed=0)
 
@@ -64,6 +73,7 @@ def test_y_buffer_reuse_and_repeatability():
                                    S.MoEShape("gather_wide_t200", T=200, d=1024, E=32, topk=8, H=256),
                                    S.MoEShape("gather_wide_t480_s2", T=480, d=512, E=32, topk=8, H=384, n_shared=2),
                                    S.MoEShape("gather_t48_s2", T=48, d=512, E=32, topk=8, H=384, n_shared=2),
+                                   S.MoEShape("wide_t100_s2", T=100, d=512, E=32, topk=8, H=384, n_shared=2),
                                    S.MoEShape("gather_t1", T=1, d=256, E=16, topk=4, H=128)])
 def test_one_call_layer_equals_the_separate_calls(shape):
     # in the decode regime moe_layer_forward's gate/up kernel gathers each token's
