@@ -47,12 +47,12 @@ __device__ __forceinline__ void div_by_scale(const float (&x)[N], float s, float
 
 // Half a warp per 128-wide group (lane l of the half holds elements 8l..8l+7, one
 // 16-byte load of bf16), two groups per warp and kQuantPairs pairs per loop trip, so
-// each warp has four groups' loads in flight. Groups are numbered row-major (group g
+// each warp has eight groups' loads in flight. Groups are numbered row-major (group g
 // of row r is r * cols/128 + g); trip j of warp w takes the pairs of groups
 // 2 (w + (j * kQuantPairs + u) * nwarps) + half, u < kQuantPairs.
 // s = amax / 448 (IEEE fp32 division), q = e4m3(x / s) (x / s correctly rounded,
 // RNE to e4m3, saturating); amax = 0 gives s = 0 and zero codes.
-constexpr int kQuantPairs = 2;
+constexpr int kQuantPairs = 4;
 
 template <bool kBf16In>
 __global__ void quant_1x128_kernel(const void *__restrict__ in, int64_t rows, int cols,
