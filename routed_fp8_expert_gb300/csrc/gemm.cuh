@@ -68,6 +68,7 @@ constexpr int kActBoxRows = 16;             // smallest activation TMA box heigh
 __device__ constexpr int kActBoxHeights[kActBoxes] = {16, 32, 64, 96, 128};
 constexpr int kMaxGroups = 1032;            // routed + shared experts, padded
 constexpr int kItemQ = 4;                   // depth of the producer -> consumers item queue
+constexpr int kItemWords = 8;               // a queue entry: the item index and its decoded Item
 
 constexpr int kStageBudget = 200 * 1024;    // shared memory for the operand ring
 
@@ -293,8 +294,8 @@ template <Kind KIND, int BN> struct SmemLayout {
                                     2 * C::kScaleSlots;
     static constexpr size_t kBars = static_cast<size_t>(C::kStages) * C::kStageBytes;
     static constexpr size_t kMisc = (kBars + kNumBars * 8 + 15) & ~size_t(15);
-    static constexpr size_t kItems = kMisc + 16;                                // [kItemQ] int
-    static constexpr size_t kTp = kItems + kItemQ * 4;
+    static constexpr size_t kItems = kMisc + 16;                                // [kItemQ][kItemWords] int
+    static constexpr size_t kTp = kItems + kItemQ * kItemWords * 4;
     static constexpr size_t kRs = kTp + kMaxGroups * 4;
     static constexpr size_t kTpm = kRs + kMaxGroups * 4;                       // [kMaxGroups] multi-tile prefix
     static constexpr int kScaleStride = BN + 4;                                // floats per stage: BN act + 2 weight
@@ -403,14 +404,31 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
     const uint32_t tmem_base = *tmem_slot;
     const int n_items = total_items<BN>(args, s_tp);
 
-    // Next item for a consumer: wait for the producer's queue slot, read it,
-    // release the slot. Called by lane 0; returns -1 on give-up.
-    auto take_item = [&](int &q, uint32_t &qphase) -> int {
+    // Next item for a consumer: wait for the producer's queue slot, read the index
+    // and the item the producer decoded, release the slot. Called by lane 0; returns
+    // -1 on give-up, n_items at the end.
+    auto take_item = [&](int &q, uint32_t &qphase, Item &I) -> int {
         if (!mbar_wait(smem_u32(&item_full[q]), qphase, abort_flag, args.err, ERR_WAIT_TMA_FULL)) return -1;
-        const int it = s_items[q];
+        const volatile int *e = s_items + q * kItemWords;
+        const int it = e[0];
+        I.g = e[1];
+        I.mb = e[2];
+        I.row0 = e[3];
+        I.n = e[4];
+        I.ks = e[5];
+        I.ntiles = e[6];
         mbar_arrive(smem_u32(&item_empty[q]));
         if (++q == kItemQ) { q = 0; qphase ^= 1; }
         return it;
+    };
+    // lane 0's item to the whole warp
+    auto bcast_item = [&](Item &I) {
+        I.g = __shfl_sync(0xffffffffu, I.g, 0);
+        I.mb = __shfl_sync(0xffffffffu, I.mb, 0);
+        I.row0 = __shfl_sync(0xffffffffu, I.row0, 0);
+        I.n = __shfl_sync(0xffffffffu, I.n, 0);
+        I.ks = __shfl_sync(0xffffffffu, I.ks, 0);
+        I.ntiles = __shfl_sync(0xffffffffu, I.ntiles, 0);
     };
 
     // The weight-scale rows [num_kb] of an item's block(s).
@@ -464,13 +482,27 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         int next_static = blockIdx.x;
         while (true) {
             int it = 0, got = 1;
+            Item I{};
             if (lane == 0) {
                 got = mbar_wait(smem_u32(&item_empty[q]), qphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
                 if (got) {
-                    if (args.item_counter) it = atomicAdd(args.item_counter, 1);
-                    else { it = next_static; next_static += gridDim.x; }
-                    if (it > n_items) it = n_items;
-                    s_items[q] = it;
+                    // the item is decoded here, once, and handed to the other roles with
+                    // its index; one that does not decode is recorded and skipped
+                    while (true) {
+                        if (args.item_counter) it = atomicAdd(args.item_counter, 1);
+                        else { it = next_static; next_static += gridDim.x; }
+                        if (it >= n_items) { it = n_items; break; }
+                        if (decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) break;
+                        record_error(args.err, ERR_BAD_TILE);
+                    }
+                    volatile int *e = s_items + q * kItemWords;
+                    e[0] = it;
+                    e[1] = I.g;
+                    e[2] = I.mb;
+                    e[3] = I.row0;
+                    e[4] = I.n;
+                    e[5] = I.ks;
+                    e[6] = I.ntiles;
                     mbar_arrive(smem_u32(&item_full[q]));
                 }
             }
@@ -478,11 +510,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             it = __shfl_sync(0xffffffffu, it, 0);
             if (!got || it >= n_items) break;
             if (++q == kItemQ) { q = 0; qphase ^= 1; }
-            Item I;
-            if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) {
-                if (lane == 0) record_error(args.err, ERR_BAD_TILE);
-                continue;
-            }
+            bcast_item(I);
             int kb0, kb1;
             kb_range(args, I, kb0, kb1);
             // one activation box per stage
@@ -570,10 +598,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             uint32_t qphase = 0;
             bool ok = true;
             while (ok) {
-                const int it = take_item(q, qphase);
-                if (it < 0 || it >= n_items) break;
                 Item I;
-                if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) continue;
+                const int it = take_item(q, qphase, I);
+                if (it < 0 || it >= n_items) break;
                 int kb0, kb1;
                 kb_range(args, I, kb0, kb1);
                 // swap-AB: M = 128 weight rows, N = the tile's tokens rounded up to 16;
@@ -638,11 +665,11 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         bool ok = true;
         while (ok) {
             int it = 0;
-            if (lane == 0) it = take_item(q, qphase);
+            Item I{};
+            if (lane == 0) it = take_item(q, qphase, I);
             it = __shfl_sync(0xffffffffu, it, 0);
             if (it < 0 || it >= n_items) break;
-            Item I;
-            if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) continue;
+            bcast_item(I);
             const float *ws0, *ws1;
             weight_scale_rows(I, ws0, ws1);
             for (int kb = 0; kb < args.num_kb; ++kb) {
@@ -673,11 +700,11 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         bool ok = true;
         while (ok) {
             int it = 0;
-            if (lane == 0) it = take_item(q, qphase);
+            Item I{};
+            if (lane == 0) it = take_item(q, qphase, I);
             it = __shfl_sync(0xffffffffu, it, 0);
             if (it < 0 || it >= n_items) break;
-            Item I;
-            if (!decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) continue;
+            bcast_item(I);
             const int n_my = max(0, min(HC, I.n - col_base));
             if constexpr (C::kWide) {
                 // token-major, 256 weight rows: thread = token row r; its HC accumulators are
