@@ -185,9 +185,12 @@ struct Item {
 // the (i - m)-th single-tile item. Under skewed routing the HBM streaming of the
 // cold experts then overlaps the hot experts' MMAs instead of alternating with them.
 // s_tpm[g] is the multi-tile prefix; the single-tile prefix is s_tp[g] - s_tpm[g].
+// Called by a whole warp (the producer's), all lanes with the same it; they
+// return the same item. The group search takes two rounds of 32 parallel
+// shared-memory reads and a ballot each, not a binary search of dependent reads.
 template <int BN>
 __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int *s_tp,
-                                            const int *s_rs, const int *s_tpm, Item &o) {
+                                            const int *s_rs, const int *s_tpm, Item &o, int lane) {
     const int nblk = a.num_mb;   // weight blocks per group
     int mbx;
     if (a.single_rows >= 0) {
@@ -209,20 +212,24 @@ __device__ __forceinline__ bool decode_item(int it, const GemmArgs &a, const int
         if (a.interleave) {
             const long long n_all = static_cast<long long>(nblk) * s_tp[a.G];
             const long long n_multi = static_cast<long long>(nblk) * s_tpm[a.G];
-            const long long m0 = static_cast<long long>(it) * n_multi / n_all;
-            const long long m1 = static_cast<long long>(it + 1) * n_multi / n_all;
-            if (m1 > m0) { idx = static_cast<int>(m0); stream = 1; }
+            const long long num = static_cast<long long>(it) * n_multi;
+            const long long m0 = num / n_all;
+            // floor((it + 1) NM / N) = m0 + [r + NM >= N] with r = it NM - m0 N < N, as NM <= N
+            if (num - m0 * n_all + n_multi >= n_all) { idx = static_cast<int>(m0); stream = 1; }
             else { idx = it - static_cast<int>(m0); stream = 2; }
         }
         // the stream's tile prefix at group g
         auto prefix = [&](int g) -> int { return stream == 0 ? s_tp[g] : stream == 1 ? s_tpm[g] : s_tp[g] - s_tpm[g]; };
         const int key = idx / nblk;
-        int lo = 0, hi = a.G;  // find the last g with prefix(g) <= key (a group of the stream)
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (prefix(mid) <= key) lo = mid; else hi = mid;
-        }
-        const int g = lo;
+        // the last g < G with prefix(g) <= key (a group of the stream): prefix rises from
+        // prefix(0) = 0, so the lanes whose candidate passes form a run from lane 0.
+        // First the chunk of 32 groups (chunk 32 only when G > 1024), then the group
+        const unsigned m1 = __ballot_sync(0xffffffffu, 32 * lane < a.G && prefix(32 * lane) <= key);
+        int c = 31 - __clz(m1);
+        if (c == 31 && a.G > 1024 && prefix(1024) <= key) c = 32;
+        const int g0 = 32 * c;
+        const unsigned m2 = __ballot_sync(0xffffffffu, g0 + lane < a.G && prefix(g0 + lane) <= key);
+        const int g = g0 + 31 - __clz(m2);
         const int nt_g = prefix(g + 1) - prefix(g);
         if (nt_g <= 0) return false;
         const int li = idx - nblk * prefix(g);
@@ -483,34 +490,34 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         while (true) {
             int it = 0, got = 1;
             Item I{};
-            if (lane == 0) {
-                got = mbar_wait(smem_u32(&item_empty[q]), qphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
-                if (got) {
-                    // the item is decoded here, once, and handed to the other roles with
-                    // its index; one that does not decode is recorded and skipped
-                    while (true) {
-                        if (args.item_counter) it = atomicAdd(args.item_counter, 1);
-                        else { it = next_static; next_static += gridDim.x; }
-                        if (it >= n_items) { it = n_items; break; }
-                        if (decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I)) break;
-                        record_error(args.err, ERR_BAD_TILE);
-                    }
-                    volatile int *e = s_items + q * kItemWords;
-                    e[0] = it;
-                    e[1] = I.g;
-                    e[2] = I.mb;
-                    e[3] = I.row0;
-                    e[4] = I.n;
-                    e[5] = I.ks;
-                    e[6] = I.ntiles;
-                    mbar_arrive(smem_u32(&item_full[q]));
-                }
-            }
+            if (lane == 0) got = mbar_wait(smem_u32(&item_empty[q]), qphase ^ 1, abort_flag, args.err, ERR_WAIT_SMEM_EMPTY);
             got = __shfl_sync(0xffffffffu, got, 0);
-            it = __shfl_sync(0xffffffffu, it, 0);
-            if (!got || it >= n_items) break;
+            if (!got) break;
+            // the item is decoded here, once, by the whole warp, and handed to the other
+            // roles with its index; one that does not decode is recorded and skipped
+            while (true) {
+                if (lane == 0) {
+                    if (args.item_counter) it = atomicAdd(args.item_counter, 1);
+                    else { it = next_static; next_static += gridDim.x; }
+                }
+                it = __shfl_sync(0xffffffffu, it, 0);
+                if (it >= n_items) { it = n_items; break; }
+                if (decode_item<BN>(it, args, s_tp, s_rs, s_tpm, I, lane)) break;
+                if (lane == 0) record_error(args.err, ERR_BAD_TILE);
+            }
+            if (lane == 0) {
+                volatile int *e = s_items + q * kItemWords;
+                e[0] = it;
+                e[1] = I.g;
+                e[2] = I.mb;
+                e[3] = I.row0;
+                e[4] = I.n;
+                e[5] = I.ks;
+                e[6] = I.ntiles;
+                mbar_arrive(smem_u32(&item_full[q]));
+            }
+            if (it >= n_items) break;
             if (++q == kItemQ) { q = 0; qphase ^= 1; }
-            bcast_item(I);
             int kb0, kb1;
             kb_range(args, I, kb0, kb1);
             // one activation box per stage
