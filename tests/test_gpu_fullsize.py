@@ -75,6 +75,13 @@ def _check_workload(shape, ex, seed, pin_layer=False):
     # the one-call layer (at decode: activation rows gathered by the gate/up kernel)
     # and the chain of separate calls (the permutation's copy) give the same bits
     assert torch.equal(y, y_chain)
+    # the one-pass quantise + permute call: the same outputs as the two calls
+    fused = moe.quant_permute_fp8(idx, xd, cfg)
+    torch.cuda.synchronize()
+    for a, f in zip((offsets, sorted_tok, inv_pos, xq_perm, sx_perm), fused):
+        assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                           f.view(torch.int32) if f.dtype == torch.float32 else f)
+    del fused
 
     # routing and permutation of all tokens
     xf = x.float().numpy()
