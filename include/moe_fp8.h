@@ -209,10 +209,15 @@ int moe_combine_residual_rmsnorm(const void *o, const float *topk_w, const int32
                                  const moe_cfg_t *cfg, int T, const void *residual, const void *gamma,
                                  float eps, void *h_out, void *x_next, void *stream);
 
-/* The whole layer: route, quantise x, permute, grouped expert GEMMs, combine.
+/* The whole layer: route, quantise x, permute, grouped expert GEMMs, combine
+ * (the quantisation runs inside the permutation, as in moe_quant_permute_fp8).
  * x [T, d] bf16; w_gate [E, d] bf16; bias [E] fp32; weights as in
  * moe_expert_gemm_fp8; y [T, d] bf16. topk_idx / topk_w [T, topk] receive the
- * routing when not NULL. workspace: moe_workspace_bytes(cfg, T) bytes. */
+ * routing when not NULL. workspace: moe_workspace_bytes(cfg, T) bytes. y equals
+ * the chain moe_route, moe_quant_fp8_1x128, moe_permute, moe_expert_gemm_fp8,
+ * moe_combine on the same inputs bit for bit. The call only enqueues kernels on
+ * the stream (no allocation, synchronisation or host read of device data), so it
+ * can be captured in a CUDA graph. */
 int moe_layer_forward(const void *x, const void *w_gate, const float *bias,
                       const uint8_t *w13, const float *w13_s, const uint8_t *w2, const float *w2_s,
                       const moe_cfg_t *cfg, int T, void *y, int32_t *topk_idx, float *topk_w,
