@@ -65,6 +65,9 @@ typedef struct {
     int H;              /* hidden features of one expert (moe_intermediate_size) */
     int n_shared;       /* always-on shared experts (n_shared_experts) */
     float route_scale;  /* routed_scaling_factor */
+    int w_tiled;        /* 0: expert weights row-major (w13 [E+S, 2, H, d], w2 [E+S, d, H]);
+                           1: the same bytes in 128 x 128 tiles, as moe_pack_weights_fp8 writes
+                           them (the GEMMs then read each 16 KB tile in one sequential run) */
 } moe_cfg_t;
 
 /* Rows of the permuted activation buffer: topk*T routed rows, then n_shared*T
@@ -116,6 +119,19 @@ int moe_permute(const int32_t *topk_idx, const uint8_t *xq, const float *sx,
                 uint8_t *xq_perm, float *sx_perm,
                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* The tiled weight layout (cfg->w_tiled = 1): w [groups, rows, cols] e4m3,
+ * row-major, becomes w_tiled [groups, rows/128, cols/128, 128, 128] with
+ *   w_tiled[g][rb][cb][r][c] = w[g][rb*128 + r][cb*128 + c],
+ * so every 128 x 128 block of a weight matrix (one 128-row block of one 128-wide
+ * K block, the unit the GEMMs load) is 16 KB of contiguous memory. For the
+ * expert weights: w13 [E+S, 2, H, d] with groups = 2(E+S), rows = H, cols = d;
+ * w2 [E+S, d, H] with groups = E+S, rows = d, cols = H. The block scales keep
+ * their layout. A one-time transformation of the weights; w and w_tiled must not
+ * overlap. rows % 128 == 0, cols % 128 == 0; groups == 0 is a no-op. Pointers
+ * 16-byte aligned. */
+int moe_pack_weights_fp8(const uint8_t *w, int64_t groups, int rows, int cols, uint8_t *w_tiled,
+                         void *stream);
+
 /* moe_quant_fp8_1x128 of x (in_is_bf16 = 1, s_transposed = 0) followed by
  * moe_permute, in one pass over x: each token's 1x128 codes and scales are
  * computed once and written straight to its permuted rows, and the unpermuted
@@ -160,6 +176,7 @@ int moe_permute_noalloc(const int32_t *topk_idx, const uint8_t *xq, const float 
  * xq_perm, sx_perm  as written by moe_permute; offsets [E+1] (device)
  * w13    [E+S, 2, H, d] e4m3 (index 0 gate_proj, 1 up_proj); w13_s [E+S, 2, H/128, d/128] fp32
  * w2     [E+S, d, H] e4m3 (down_proj); w2_s [E+S, d/128, H/128] fp32
+ *        (w13 and w2 in the tiled layout of moe_pack_weights_fp8 when cfg->w_tiled = 1)
  * o      [moe_permuted_rows, d] bf16, same row order as xq_perm
  * Routed experts come first, shared experts last. */
 int moe_expert_gemm_fp8(const uint8_t *xq_perm, const float *sx_perm, const int32_t *offsets,

@@ -22,7 +22,7 @@ _c_int, _c_size, _c_i64, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_int64, ct
 
 class MoeCfg(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("E", ctypes.c_int), ("topk", ctypes.c_int), ("H", ctypes.c_int),
-                ("n_shared", ctypes.c_int), ("route_scale", ctypes.c_float)]
+                ("n_shared", ctypes.c_int), ("route_scale", ctypes.c_float), ("w_tiled", ctypes.c_int)]
 
 
 # name -> (restype, argtypes)
@@ -30,6 +30,7 @@ _SIGS = {
     "moe_permuted_rows": (_c_i64, [ctypes.POINTER(MoeCfg), _c_int]),
     "moe_workspace_bytes": (_c_size, [ctypes.POINTER(MoeCfg), _c_int]),
     "moe_quant_fp8_1x128": (_c_int, [_vp, _c_int, _c_i64, _c_int, _vp, _vp, _c_int, _vp]),
+    "moe_pack_weights_fp8": (_c_int, [_vp, _c_i64, _c_int, _c_int, _vp, _vp]),
     "moe_route": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_permute": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(MoeCfg), _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                              _c_size, _vp]),
@@ -101,8 +102,21 @@ def _cuda(*ts):
             raise ValueError("tensors must be on a CUDA device")
 
 
-def cfg_of(shape) -> MoeCfg:
-    return MoeCfg(shape.d, shape.E, shape.topk, shape.H, shape.n_shared, shape.route_scale)
+def cfg_of(shape, w_tiled: bool = False) -> MoeCfg:
+    return MoeCfg(shape.d, shape.E, shape.topk, shape.H, shape.n_shared, shape.route_scale, int(w_tiled))
+
+
+def pack_weights_fp8(w: torch.Tensor) -> torch.Tensor:
+    """moe_pack_weights_fp8: e4m3 weights [..., rows, cols] (row-major, uint8) into
+    the tiled layout [groups, rows/128, cols/128, 128, 128] (groups = the product of
+    the leading dimensions); returned flat in w's shape."""
+    _cuda(w)
+    w = w.contiguous()
+    rows, cols = w.shape[-2], w.shape[-1]
+    groups = w.numel() // (rows * cols)
+    out = torch.empty_like(w)
+    _check(load().moe_pack_weights_fp8(_p(w), groups, rows, cols, _p(out), _stream(w.device)))
+    return out
 
 
 def permuted_rows(cfg: MoeCfg, T: int) -> int:

@@ -56,6 +56,7 @@ int check_cfg(const moe_cfg_t *c) {
         return fail(MOE_ERR_UNSUPPORTED, "E=%d must be in [topk, 1024]", c->E);
     if (c->n_shared < 0 || c->n_shared > 4) return fail(MOE_ERR_UNSUPPORTED, "n_shared=%d must be in [0, 4]", c->n_shared);
     if (!std::isfinite(c->route_scale)) return fail(MOE_ERR_ARG, "route_scale is not finite");
+    if (c->w_tiled != 0 && c->w_tiled != 1) return fail(MOE_ERR_ARG, "w_tiled=%d must be 0 or 1", c->w_tiled);
     return MOE_OK;
 }
 
@@ -281,6 +282,47 @@ int make_act_maps_kpair(ActMaps *m, const void *ptr, uint64_t rows, uint64_t col
     return MOE_OK;
 }
 
+// The tiled weight layout [groups][rows/128][cols/128][128][128] as a map whose two
+// innermost dimensions are one 128 x 128 tile (x = the 128 bytes of a tile row,
+// y = its 128 rows, z = the K block, w = the row block over all groups).
+// pair_rows: box {128, 128, 1, 2}, two row blocks of a K block (256-row items);
+// otherwise box {128, 128, 2, 1}, two K blocks of a row block (the K-pair kind).
+int make_map_tiled_w2(CUtensorMap *m, const void *ptr, uint64_t groups, uint64_t rows, uint64_t cols,
+                      bool pair_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[4] = {128, 128, cols / 128, groups * (rows / 128)};
+    cuuint64_t strides[3] = {128, 16384, 16384 * (cols / 128)};
+    cuuint32_t box[4] = {128, 128, pair_rows ? 1u : 2u, pair_rows ? 2u : 1u};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (tiled 4D) failed (%d)", static_cast<int>(r));
+    return MOE_OK;
+}
+
+// The tiled gate/up weights [2G][H/128][d/128][128][128] as a 5D map (x, y = a
+// tile's bytes and rows, z = K block, w = row block, v = 2g + gate/up) whose box
+// {128, 128, 1, 1, 2} holds a gate tile and the up tile of the same rows.
+int make_map_tiled_gateup(CUtensorMap *m, const void *ptr, uint64_t G, uint64_t H, uint64_t d) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[5] = {128, 128, d / 128, H / 128, 2 * G};
+    cuuint64_t strides[4] = {128, 16384, 16384 * (d / 128), 16384 * (d / 128) * (H / 128)};
+    cuuint32_t box[5] = {128, 128, 1, 1, 2};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (tiled 5D) failed (%d)", static_cast<int>(r));
+    return MOE_OK;
+}
+
+int gateup_map(CUtensorMap *m, const void *w13, const moe_cfg_t &c, uint64_t G) {
+    return c.w_tiled ? make_map_tiled_gateup(m, w13, G, c.H, c.d) : make_map_gateup(m, w13, G, c.H, c.d);
+}
+
 // ---------------------------------------------------------------- steps
 
 int route_impl(const void *x, const void *wg, const float *bias, const moe_cfg_t &c, int T, int32_t *idx,
@@ -328,7 +370,7 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     }
     CUtensorMap m13;
     ActMaps mx;
-    MOE_CHECK(make_map(&m13, w13, 1, static_cast<uint64_t>(G) * 2 * c.H, c.d, kBM));
+    MOE_CHECK(gateup_map(&m13, w13, c, G));
     MOE_CHECK(make_act_maps(&mx, xq_perm, 1, R, c.d));
     GemmArgs gu{};
     gu.G = G;
@@ -341,11 +383,11 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     gu.act_scale_t = sx_perm;
     gu.w_scale = w13_s;
     gu.a_rows_per_group = 2 * c.H;
+    gu.w_tiled = c.w_tiled;
     if (decode_regime(c, T)) {
         // fused gate/up + SiLU*mul + h quantisation; items handed out by the global
         // counter (one atomic per 56-K-block item), so the CTAs that finish early
         // share the last partial round
-        MOE_CHECK(make_map_gateup(&m13, w13, G, c.H, c.d));
         gu.hq = hq;
         gu.hs_t = hs;
         gu.item_counter = ws.counters;
@@ -362,7 +404,6 @@ int gateup_impl(const uint8_t *xq_perm, const float *sx_perm, const int32_t *off
     }
     // 128-token tiles, token-major: the gate and up blocks of 128 features per
     // item (N = 256) with the fused SiLU*mul and h quantisation
-    MOE_CHECK(make_map_gateup(&m13, w13, G, c.H, c.d));
     gu.hq = hq;
     gu.hs_t = hs;
     gu.item_counter = ws.counters;
@@ -402,21 +443,25 @@ int down_impl(const uint8_t *hq, const float *hs, const int32_t *offsets, const 
     dn.w_scale = w2_s;
     dn.a_rows_per_group = c.d;
     dn.out = static_cast<__nv_bfloat16 *>(o);
+    dn.w_tiled = c.w_tiled;
     // (plain item order: interleaving multi-tile and one-tile experts' items, as the
     // gate/up GEMM does, measured 3% slower here at the prefill and skewed40 batches)
     if (down_pair(c, T)) {
         // decode: two adjacent 128-row blocks per item, one 256-row box (32 KB of
         // weights per K block and request)
-        MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
+        if (c.w_tiled) MOE_CHECK(make_map_tiled_w2(&m2, w2, G, c.d, c.H, true));
+        else MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
         dn.num_mb = c.d / 256;
         MOE_CUDA(launch_grouped_gemm(Kind::DownPair, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     } else if ((c.d / 128) % 2 == 0) {
         // 128-token tiles, token-major, two 128-row blocks per item (N = 256)
-        MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
+        if (c.w_tiled) MOE_CHECK(make_map_tiled_w2(&m2, w2, G, c.d, c.H, true));
+        else MOE_CHECK(make_map(&m2, w2, 1, static_cast<uint64_t>(G) * c.d, c.H, 2 * kBM));
         dn.num_mb = c.d / 256;
         MOE_CUDA(launch_grouped_gemm(Kind::DownWide, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     } else {
-        MOE_CHECK(make_map_kpair(&m2, w2, static_cast<uint64_t>(G) * c.d, c.H, kBM));
+        if (c.w_tiled) MOE_CHECK(make_map_tiled_w2(&m2, w2, G, c.d, c.H, false));
+        else MOE_CHECK(make_map_kpair(&m2, w2, static_cast<uint64_t>(G) * c.d, c.H, kBM));
         MOE_CHECK(make_act_maps_kpair(&mh, hq, R, c.H));
         MOE_CUDA(launch_grouped_gemm(Kind::Down, bn, m2, mh, dn, num_sms(), st), "down GEMM launch");
     }
@@ -462,6 +507,23 @@ int moe_quant_fp8_1x128(const void *in, int in_is_bf16, int64_t rows, int cols, 
     MOE_CUDA(launch_quant(in, in_is_bf16 != 0, rows, cols, q, s, s_transposed != 0, num_sms(),
                           static_cast<cudaStream_t>(stream)),
              "quantise launch");
+    t_launches = 1;
+    return MOE_OK;
+}
+
+int moe_pack_weights_fp8(const uint8_t *w, int64_t groups, int rows, int cols, uint8_t *w_tiled, void *stream) {
+    t_launches = 0;
+    if (groups < 0) return fail(MOE_ERR_ARG, "groups=%lld is negative", static_cast<long long>(groups));
+    if (rows <= 0 || rows % 128 || cols <= 0 || cols % 128)
+        return fail(MOE_ERR_UNSUPPORTED, "rows=%d and cols=%d must be positive multiples of 128", rows, cols);
+    if (groups == 0) return MOE_OK;
+    MOE_CHECK(check_ptr(w, "w"));
+    MOE_CHECK(check_ptr(w_tiled, "w_tiled"));
+    const uint64_t bytes = static_cast<uint64_t>(groups) * rows * cols;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(w), b = reinterpret_cast<uintptr_t>(w_tiled);
+    if (a < b + bytes && b < a + bytes) return fail(MOE_ERR_ARG, "w and w_tiled overlap");
+    MOE_CUDA(launch_pack_tiles(w, groups, rows, cols, w_tiled, num_sms(), static_cast<cudaStream_t>(stream)),
+             "weight tiling launch");
     t_launches = 1;
     return MOE_OK;
 }

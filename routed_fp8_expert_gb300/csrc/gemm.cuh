@@ -133,6 +133,9 @@ struct GemmArgs {
     int interleave;           // merge the items of multi-tile groups with those of one-tile groups
     const float *act_scale_t; // [num_kb][total_rows]  (FP8 kinds)
     const float *w_scale;     // GateUp: [G][2][num_mb][num_kb]; Down: [G][num_mb][num_kb]
+    int w_tiled;              // map_a is over the tiled weight layout (128 x 128 tiles): gate/up 5D
+                              // {128 B, 128 rows, K block, row block, 2G}; down 4D {128 B, 128 rows,
+                              // K block, row block} (expert kinds only)
     int a_rows_per_group;     // weight rows of one group in the A tensor map (GateUp: 2*H, Down: d_out)
     uint8_t *hq;              // GateUp: [total_rows][num_mb*128]
     float *hs_t;              // GateUp: [num_mb][total_rows]
@@ -562,7 +565,8 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     cp_async_arrive_noinc(fb);
                     if (lane == 0) {
                         mbar_arrive_expect_tx(fb, bytes);
-                        tma_load_3d(sbase, &map_a, fb, kb * kKbElems, I.mb * kBM, 2 * I.g, pol_w);
+                        if (args.w_tiled) tma_load_5d(sbase, &map_a, fb, 0, 0, kb, I.mb, 2 * I.g, pol_w);
+                        else tma_load_3d(sbase, &map_a, fb, kb * kKbElems, I.mb * kBM, 2 * I.g, pol_w);
                     }
                 } else if (lane == 0) {
                     mbar_arrive_expect_tx(fb, bytes);
@@ -572,14 +576,23 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                     // K-pair kinds: K blocks kb and kb+1 of the weight rows and of the
                     // activation rows, one request each (x = 0, y = row, z = K block)
                     if constexpr (C::kKPS == 2) {
-                        tma_load_3d(sbase, &map_a, fb, 0, arow0, kb, pol_w);
+                        // tiled: box {128, 128, 2 K blocks, 1}, two consecutive tiles
+                        if (args.w_tiled) tma_load_4d(sbase, &map_a, fb, 0, 0, kb, arow0 / kBM, pol_w);
+                        else tma_load_3d(sbase, &map_a, fb, 0, arow0, kb, pol_w);
                         tma_load_3d(sbase + C::kAStageBytes, &map_b.box[box_i], fb, 0, I.row0, kb, pol_x);
                     } else {
                         const int kx = kb * kKbElems;
-                        if constexpr (KIND == Kind::GateUp || KIND == Kind::GateUpWide)
-                            tma_load_3d(sbase, &map_a, fb, kx, I.mb * kBM, 2 * I.g, pol_w);
-                        else
+                        if constexpr (KIND == Kind::GateUp || KIND == Kind::GateUpWide) {
+                            // tiled: box {128, 128, 1, 1, 2}, the gate and up tiles
+                            if (args.w_tiled) tma_load_5d(sbase, &map_a, fb, 0, 0, kb, I.mb, 2 * I.g, pol_w);
+                            else tma_load_3d(sbase, &map_a, fb, kx, I.mb * kBM, 2 * I.g, pol_w);
+                        } else if constexpr (KIND == Kind::DownPair || KIND == Kind::DownWide) {
+                            // tiled: box {128, 128, 1, 2}, two row blocks' tiles
+                            if (args.w_tiled) tma_load_4d(sbase, &map_a, fb, 0, 0, kb, arow0 / kBM, pol_w);
+                            else tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
+                        } else {
                             tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
+                        }
                         tma_load_2d(sbase + C::kAStageBytes, &map_b.box[box_i], fb, kx, I.row0, pol_x);
                     }
                 }

@@ -56,6 +56,8 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
                            float *sx_perm, int *launches,
                            cudaStream_t stream, bool copy_rows = true, const void *x_bf16 = nullptr,
                            uint8_t *xq_out = nullptr, float *sx_out = nullptr);
+cudaError_t launch_pack_tiles(const uint8_t *w, int64_t groups, int rows, int cols, uint8_t *w_tiled, int num_sms,
+                              cudaStream_t stream);
 cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
                          int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b, int32_t *counters,
                          cudaStream_t stream);

@@ -77,6 +77,16 @@ cudaError_t launch_permute(const int32_t *idx, const uint8_t *xq, const float *s
     return e;
 }
 
+cudaError_t launch_pack_tiles(const uint8_t *w, int64_t groups, int rows, int cols, uint8_t *w_tiled, int num_sms,
+                              cudaStream_t stream) {
+    const int64_t units = groups * (rows / 128) * (cols / 128) * 1024;
+    int64_t blocks = (units + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(pack_tiles_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, w, groups, rows,
+                      cols, w_tiled);
+}
+
 cudaError_t launch_sched(const int32_t *offsets, int E, int S, int T, int k, int tile_a, int tile_b,
                          int32_t *row_start, int32_t *tile_prefix_a, int32_t *tile_prefix_b, int32_t *counters,
                          cudaStream_t stream) {

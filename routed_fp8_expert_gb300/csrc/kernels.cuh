@@ -602,6 +602,30 @@ __global__ void combine_kernel(const __nv_bfloat16 *__restrict__ o, const float 
     reinterpret_cast<uint4 *>(y + static_cast<size_t>(t) * d)[v] = out;
 }
 
+// ------------------------------------------------------------------ weight tiling
+// w [groups][rows][cols] -> w_tiled [groups][rows/128][cols/128][128][128]:
+// w_tiled[g][rb][cb][r][c] = w[g][rb*128 + r][cb*128 + c]. Grid-stride over the
+// 16-byte units of the output (8 per tile row), read from the input row.
+__global__ void pack_tiles_kernel(const uint8_t *__restrict__ w, int64_t groups, int rows, int cols,
+                                  uint8_t *__restrict__ w_tiled) {
+    pdl_trigger();
+    pdl_wait();
+    const int rbs = rows / 128, cbs = cols / 128;
+    const int64_t units = groups * rbs * cbs * 128 * 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const int c16 = static_cast<int>(u & 7);
+        const int r = static_cast<int>((u >> 3) & 127);
+        const int64_t tile = u >> 10;   // [g][rb][cb]
+        const int cb = static_cast<int>(tile % cbs);
+        const int64_t grb = tile / cbs;  // g * rbs + rb
+        const int rb = static_cast<int>(grb % rbs);
+        const int64_t g = grb / rbs;
+        const uint8_t *src = w + (g * rows + static_cast<int64_t>(rb) * 128 + r) * cols + static_cast<int64_t>(cb) * 128 + c16 * 16;
+        reinterpret_cast<uint4 *>(w_tiled)[u] = *reinterpret_cast<const uint4 *>(src);
+    }
+}
+
 // ------------------------------------------------------------------ bounded-wait self-test
 // One CTA of two warps whose lane 0s wait on an mbarrier that nothing arrives at,
 // through the GEMMs' own bounded wait: warp 0 with the given limit, warp 1 with the

@@ -179,6 +179,22 @@ def test_fullsize_skewed40(kimi_weights):
     assert 0.3 < float(np.isin(idx, S.SKEWED40.hot_experts).mean()) < 0.5
 
 
+@pytest.mark.parametrize("shape", [S.DECODE, S.PREFILL, S.SKEWED], ids=lambda s: s.name)
+def test_fullsize_tiled_weights_equal_row_major(kimi_weights, shape):
+    # the same layer with the weights in the tiled layout (moe_pack_weights_fp8):
+    # every GEMM kind of the workload reads its tiles, and y is the same bit for bit
+    x = S.gen_x(shape.T, shape.d, seed=5).to(DEV)
+    wg, b = (t.to(DEV) for t in S.gen_router(shape, seed=5))
+    ex = kimi_weights
+    ext = S.ExpertWeights(moe.pack_weights_fp8(ex.w13), ex.w13_s, moe.pack_weights_fp8(ex.w2), ex.w2_s)
+    y = moe.layer_forward(x, wg, b, ex, moe.cfg_of(shape))
+    yt = moe.layer_forward(x, wg, b, ext, moe.cfg_of(shape, w_tiled=True))
+    torch.cuda.synchronize()
+    moe.check_device_error(DEV)
+    assert torch.equal(y, yt)
+    del ext
+
+
 def test_fullsize_dense():
     # the first block's dense FFN, T=8192: 64 tokens including the two sides of the
     # first 128-token tile boundary and the last token
