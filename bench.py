@@ -61,18 +61,18 @@ DATA = ("synthetic, seeded: x ~ N(0,1) bf16; W_g ~ N(0,0.02) bf16; bias ~ N(0,0.
 
 # DRAM bytes (read + write) per launch of the decode gate/up kernel, from one ncu
 # capture of the same kernel on the decode-like case of a few GB (decode_e64:
-# 1.9163 GB of traffic for 1.9092 GB of algorithmic and 4.1 MB of implementation
+# 1.9155 GB of traffic for 1.9092 GB of algorithmic and 4.1 MB of implementation
 # bytes). Traffic grows with the touched experts' weights, so the full launch's
 # figure is this ratio times its algorithmic plus implementation bytes. Keyed by the
 # hash of the kernel sources at capture time: once the sources change, the figure no
 # longer applies (null).
-NCU_TRAFFIC = {"ratio": 1.0015, "src": "6d9ab3355a7be612", "case": "decode_e64"}
+NCU_TRAFFIC = {"ratio": 1.0011, "src": "3fd93919befbe3a5", "case": "decode_e64"}
 # The same for the token-major gate/up kernel in the one-tile-per-expert regime of
 # the prefill batch (prefill_e64: 96 rows per routed expert, so one 128-token tile;
-# 1.9944 GB of traffic for 1.9146 GB of algorithmic and 65.7 MB of implementation
+# 1.9724 GB of traffic for 1.9146 GB of algorithmic and 65.7 MB of implementation
 # bytes), applied to workloads without hot experts and with at most 128 rows per
 # routed expert.
-NCU_TRAFFIC_WIDE = {"ratio": 1.0071, "src": "6d9ab3355a7be612", "case": "prefill_e64"}
+NCU_TRAFFIC_WIDE = {"ratio": 0.9960, "src": "3fd93919befbe3a5", "case": "prefill_e64"}
 
 
 def kernel_src_hash() -> str:
@@ -282,6 +282,7 @@ def workload_config(shape) -> dict:
                 "l2": "inputs larger than L2 (0.40 GB of FP8 weights + 59 MB of activations per step)"}
     cfg = {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "topk": shape.topk, "H": shape.H,
            "n_shared": shape.n_shared, "route_scale": shape.route_scale,
+           "weight_layout": "tiled 128x128 (moe_pack_weights_fp8, once before timing)",
            "l2": f"inputs larger than L2 ({(shape.E + shape.n_shared) * 3 * shape.d * shape.H / 1e9:.2f} GB of "
                  f"FP8 expert weights per step)"}
     if shape.hot_experts:
@@ -383,13 +384,19 @@ def cpu_baseline_moe(shape, x, wg, b, ex, idx, n_tokens, seed):
             "sample": f"{len(toks)} of {shape.T} tokens through the fp64 oracle ({dt:.1f} s)"}
 
 
-def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
+def run_moe(args, shape, rank, local, world, dev, peaks, ex=None, ext=None):
+    """ex: the expert weights (row-major; the CPU baseline decodes them); ext: the
+    same weights in the tiled layout, which every GPU call of the step reads."""
     import routed_fp8_expert_gb300 as moe
-    cfg = moe.cfg_of(shape)
+    cfg = moe.cfg_of(shape, w_tiled=True)
     T, d, H, k, E, Sh = shape.T, shape.d, shape.H, shape.topk, shape.E, shape.n_shared
     R = (k + Sh) * T
     if ex is None:
         ex = S.gen_experts(E + Sh, d, H, seed=args.seed, device=dev)
+    if ext is None:
+        # the one-time weight preparation, before any timing
+        ext = S.ExpertWeights(moe.pack_weights_fp8(ex.w13), ex.w13_s, moe.pack_weights_fp8(ex.w2), ex.w2_s)
+        torch.cuda.synchronize(dev)
     x = S.gen_x(T, d, seed=args.seed + rank, device=dev)
     wg, b = S.gen_router(shape, seed=args.seed, device=dev)
     ws = moe.workspace(cfg, T, dev)
@@ -433,10 +440,10 @@ def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
         n += call(L.moe_quant_permute_fp8(P(idx), P(x), cref, T, P(offsets), P(sorted_tok), P(inv_pos),
                                           P(xq_perm), P(sx_perm), P(ws), nws, st))
         mark(2)
-        n += call(L.moe_expert_gateup_fp8(P(xq_perm), P(sx_perm), P(offsets), P(ex.w13), P(ex.w13_s), cref, T,
+        n += call(L.moe_expert_gateup_fp8(P(xq_perm), P(sx_perm), P(offsets), P(ext.w13), P(ext.w13_s), cref, T,
                                           P(hq), P(hs), P(ws), nws, st))
         mark(3)
-        n += call(L.moe_expert_down_fp8(P(hq), P(hs), P(offsets), P(ex.w2), P(ex.w2_s), cref, T, P(o), P(ws), nws,
+        n += call(L.moe_expert_down_fp8(P(hq), P(hs), P(offsets), P(ext.w2), P(ext.w2_s), cref, T, P(o), P(ws), nws,
                                         st))
         mark(4)
         n += call(L.moe_combine(P(o), P(w), P(inv_pos), cref, T, P(y), st))
@@ -503,12 +510,12 @@ def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
     # end to end through the one-call API, each step's x copied in from pinned host
     # memory and its y copied out, overlapped with the neighbouring steps' compute
     e2e_ms, yd = pipelined_e2e(dev, args.steps, args.warmup, x, (T, d),
-                               lambda xi, yo: moe.layer_forward(xi, wg, b, ex, cfg, ws=ws, y=yo), world)
+                               lambda xi, yo: moe.layer_forward(xi, wg, b, ext, cfg, ws=ws, y=yo), world)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e_value = tokens_total / (e2e_ms * 1e-3)
     same = torch.equal(yd, y)
     pieces = time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks)
-    pieces["moe_block_ffn_forward"] = time_block_call(moe, x, wg, b, ex, cfg, ws, dev, n=max(3, min(args.steps, 20)))
+    pieces["moe_block_ffn_forward"] = time_block_call(moe, x, wg, b, ext, cfg, ws, dev, n=max(3, min(args.steps, 20)))
     step_bytes = layer_weight_bytes + 2 * T * d * 2
 
     line = {
@@ -535,7 +542,7 @@ def run_moe(args, shape, rank, local, world, dev, peaks, ex=None):
         "clocks": clk,
         "block_pieces": pieces,
     }
-    return line, (x, wg, b, ex, idx)
+    return line, (x, wg, b, ex, idx, ext)
 
 
 def time_block_pieces(L, x, o, w, inv_pos, cfg, shape, dev, st, peaks, n=50):
@@ -741,21 +748,21 @@ def main():
     else:
         line, extra = run_moe(args, shape, rank, local, world, dev, peaks)
         if want_cpu:
-            x, wg, b, ex, idx = extra
+            x, wg, b, ex, idx, _ = extra
             line["cpu_baseline"] = cpu_baseline_moe(shape, x, wg, b, ex, idx, args.cpu_tokens, args.seed)
         if args.workload == "all":
             # every other workload, each with its own roofline, clocks, end-to-end figure
             # and oracle sample; the MoE batches reuse the step's 16.96 GB of weights
-            ex = extra[3]
+            ex, ext = extra[3], extra[5]
             wl = {}
             for name in EXTRA_WORKLOADS:
                 wshape = WORKLOADS[name]
                 if isinstance(wshape, S.DenseShape):
                     wline = run_dense(args, wshape, rank, world, dev, peaks, want_cpu=want_cpu)
                 else:
-                    wline, wextra = run_moe(args, wshape, rank, local, world, dev, peaks, ex=ex)
+                    wline, wextra = run_moe(args, wshape, rank, local, world, dev, peaks, ex=ex, ext=ext)
                     if want_cpu:
-                        x, wg, b, _, idx = wextra
+                        x, wg, b, _, idx, _ = wextra
                         wline["cpu_baseline"] = cpu_baseline_moe(wshape, x, wg, b, ex, idx, max(1, args.cpu_tokens // 2),
                                                                  args.seed)
                     del wextra
