@@ -33,7 +33,9 @@ def _check(idx, E, d=256, S=1):
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 32, 8), (33, 32, 8), (64, 32, 8), (1000, 384, 8), (4096, 384, 8),
-                                   (77, 40, 1), (50, 64, 32)])
+                                   (77, 40, 1), (50, 64, 32),
+                                   # eight full 32-token chunks, the most experts, one token into a ninth chunk
+                                   (256, 384, 8), (255, 1024, 8), (257, 384, 8)])
 def test_random_routing(T, E, k):
     _check(_random_idx(T, E, k, np.random.default_rng(T + E + k)), E)
 
