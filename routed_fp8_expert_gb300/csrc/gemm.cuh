@@ -71,6 +71,7 @@ constexpr int kItemQ = 4;                   // depth of the producer -> consumer
 constexpr int kItemWords = 8;               // a queue entry: the item index and its decoded Item
 
 constexpr int kStageBudget = 200 * 1024;    // shared memory for the operand ring
+constexpr int kPrefetchReps = 4;            // first-round items whose weights a CTA prefetches
 
 constexpr int pow2_at_least(int v, int lo) { return v <= lo ? lo : 2 * pow2_at_least((v + 1) / 2, lo); }
 
@@ -137,6 +138,18 @@ struct GemmArgs {
                               // {128 B, 128 rows, K block, row block, 2G}; down 4D {128 B, 128 rows,
                               // K block, row block} (expert kinds only)
     int a_rows_per_group;     // weight rows of one group in the A tensor map (GateUp: 2*H, Down: d_out)
+    // L2 prefetch of weights while the preceding kernel still runs (a hint; null: none).
+    // Item j of the first round is taken to be (group j / pf_items, block j % pf_items),
+    // as it is when the first groups are all routed to; its weight run(s) start at
+    // pf_base + g * pf_group_bytes + i * pf_item_bytes (and pf_second bytes further on,
+    // if non-zero), of which pf_len bytes are prefetched. Every address stays inside
+    // the weights.
+    const uint8_t *pf_base;
+    uint64_t pf_group_bytes;
+    uint64_t pf_item_bytes;
+    uint64_t pf_second;
+    uint32_t pf_len;          // a multiple of 16 KB
+    int pf_items;
     uint8_t *hq;              // GateUp: [total_rows][num_mb*128]
     float *hs_t;              // GateUp: [num_mb][total_rows]
     __nv_bfloat16 *out;       // Down: [total_rows][num_mb*128]
@@ -398,6 +411,26 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
         for (int i = 0; i < kActBoxes; ++i) tma_prefetch_desc(&map_b.box[i]);
     }
     if (warp == 1) tmem_alloc<C::kTmemCols>(smem_u32(tmem_slot));
+    // weights are not written by the preceding kernels: their first bytes may be on
+    // their way to L2 before it completes (HBM is idle during the routing and the
+    // permutation, and partly so during the previous GEMM's last items)
+    // CTA b prefetches the first-round items b + r n / kPrefetchReps (mod n, n CTAs):
+    // each item is prefetched by several CTAs, so that those resident early (on the SMs
+    // the router GEMM leaves free) cover the whole first round
+    if (warp == 0 && args.pf_base != nullptr) {
+        for (int r = 0; r < kPrefetchReps; ++r) {
+            const int item = static_cast<int>((blockIdx.x + r * (gridDim.x / kPrefetchReps)) % gridDim.x);
+            const int g = item / args.pf_items, i = item % args.pf_items;
+            if (g >= args.G) continue;
+            const uint8_t *run = args.pf_base + static_cast<uint64_t>(g) * args.pf_group_bytes +
+                                 static_cast<uint64_t>(i) * args.pf_item_bytes;
+            const int chunks = static_cast<int>(args.pf_len >> 14);
+            const int total = args.pf_second ? 2 * chunks : chunks;
+            for (int c = lane; c < total; c += 32)
+                l2_prefetch_bulk(run + (c >= chunks ? args.pf_second : 0) + (static_cast<uint64_t>(c % chunks) << 14),
+                                 16384u);
+        }
+    }
     // the set-up above touches only shared memory, TMEM and the kernel's parameters,
     // so it overlaps the preceding kernel's tail; the global inputs come after it
     pdl_wait();
