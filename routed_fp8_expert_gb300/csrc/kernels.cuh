@@ -144,10 +144,28 @@ __global__ void topk_kernel(const float *__restrict__ logits, int splits, const 
     const float *lrow = logits + static_cast<size_t>(t) * E;
     const size_t split_stride = static_cast<size_t>(T) * E;
     float sv[NPER], cv[NPER];
-    // logits: the split partials added in split order (independent loads per split)
+    // logits: the split partials added in split order; the loads of the first
+    // kGather splits are all issued before the first addition
+    constexpr int kGather = (NPER <= 12) ? 4 : 1;
 #pragma unroll
     for (int i = 0; i < NPER; ++i) sv[i] = (lane + 32 * i < E) ? lrow[lane + 32 * i] : 0.f;
-    for (int sp = 1; sp < splits; ++sp) {
+    if constexpr (kGather > 1) {
+        float pv[kGather - 1][NPER];
+#pragma unroll
+        for (int sp = 1; sp < kGather; ++sp) {
+            const float *prow = lrow + sp * split_stride;
+#pragma unroll
+            for (int i = 0; i < NPER; ++i)
+                pv[sp - 1][i] = (sp < splits && lane + 32 * i < E) ? prow[lane + 32 * i] : 0.f;
+        }
+#pragma unroll
+        for (int sp = 1; sp < kGather; ++sp)
+            if (sp < splits) {
+#pragma unroll
+                for (int i = 0; i < NPER; ++i) sv[i] += pv[sp - 1][i];
+            }
+    }
+    for (int sp = kGather; sp < splits; ++sp) {
         const float *prow = lrow + sp * split_stride;
 #pragma unroll
         for (int i = 0; i < NPER; ++i)
