@@ -36,7 +36,8 @@
 // while block kb is promoted.
 //
 // Router kind: bf16 x bf16 -> fp32, accumulated in TMEM over the whole K
-// range; the epilogue writes fp32 logits.
+// range; the epilogue writes fp32 logits. With 128-token tiles an item holds up to
+// three 128-expert blocks (three MMAs on one token tile per K step, 384 TMEM columns).
 #pragma once
 #include "internal.h"
 #include "ptx.cuh"
@@ -80,7 +81,10 @@ template <Kind K, int BN> struct KindCfg {
     // token-major with 256 weight rows per item (two 128-row tiles per K block)
     static constexpr bool kWide = (K == Kind::GateUpWide || K == Kind::DownWide);
     // weight tiles per K block: gate and up, or two row blocks
-    static constexpr int kATiles = (K == Kind::GateUp || K == Kind::DownPair || kWide) ? 2 : 1;
+    // the 128-token router reads up to three 128-row blocks of W_g per stage (all
+    // the experts of a 384-expert router: the token tile is read once, not per block)
+    static constexpr bool kRouterAll = (K == Kind::Router && BN == 128);
+    static constexpr int kATiles = kRouterAll ? 3 : (K == Kind::GateUp || K == Kind::DownPair || kWide) ? 2 : 1;
     static constexpr bool kPromote = (K != Kind::Router);         // per-128-K fp32 promotion
     static constexpr bool kBf16 = (K == Kind::Router);
     // token-major: tokens on the TMEM lanes (M = 128), weight rows on the columns
@@ -118,7 +122,7 @@ template <Kind K, int BN> struct KindCfg {
     static constexpr int kWideRegs = (16384 / ((kThreads / 32 + 3) / 4 * 32)) / 8 * 8;
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "tile width");
     static_assert(!kTM || BN == 128, "token-major tiles hold 128 tokens (the MMA M dimension)");
-    static_assert(kStages * kKPS >= 4 && kStages >= 2, "pipeline depth");
+    static_assert((kStages * kKPS >= 4 || kRouterAll) && kStages >= 3, "pipeline depth");
     static_assert(kKPS == 1 || kATiles == 1, "K-pair stages hold one weight tile per K block");
 };
 
@@ -156,6 +160,7 @@ struct GemmArgs {
     float *logits;            // Router: [k_splits][total_rows][n_valid] partial logits
     int n_valid;              // Router: valid weight rows (experts)
     int k_splits;             // Router: K range split into this many partial sums (>= 1)
+    int a_tiles;              // 128-token router: weight blocks per item (num_mb is then 1), or 0
     unsigned int *err;        // device error word (bounded waits that gave up)
     int *item_counter;        // dynamic scheduler counter (zero at launch), or null for static order
     // GateUp gathering its activation rows (null: rows of the permuted copy by TMA):
@@ -561,6 +566,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             // full boxes count toward the transaction bytes, including rows and a
             // K block beyond the tensor, which the TMA unit fills with zeros
             uint32_t bytes = C::kKPS * (C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes);
+            if constexpr (C::kRouterAll) {
+                if (args.a_tiles > 0) bytes = args.a_tiles * kATileBytes + kActBoxHeights[box_i] * kKBytes;
+            }
             // gathering GateUp: lane i copies the tile's row i (one token's 128-byte K
             // block, eight 16-byte copies into its 128-byte-swizzled place); only the
             // weights come by TMA. Rows past the tile's end stay as they are: their
@@ -623,6 +631,13 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                             // tiled: box {128, 128, 1, 2}, two row blocks' tiles
                             if (args.w_tiled) tma_load_4d(sbase, &map_a, fb, 0, 0, kb, arow0 / kBM, pol_w);
                             else tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
+                        } else if constexpr (C::kRouterAll) {
+                            if (args.a_tiles > 0) {
+                                for (int t = 0; t < args.a_tiles; ++t)
+                                    tma_load_2d(sbase + t * kATileBytes, &map_a, fb, kx, t * kBM, pol_w);
+                            } else {
+                                tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
+                            }
                         } else {
                             tma_load_2d(sbase, &map_a, fb, kx, arow0, pol_w);
                         }
@@ -687,7 +702,11 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                             const uint32_t acc = C::kPromote ? (k > 0) : (kbh > kb0 || k > 0);
                             const uint64_t bdesc = sdesc_sw128(bbase + k * 32);   // activations
                             const uint64_t adesc = sdesc_sw128(abase + k * 32);   // weights
-                            if constexpr (C::kBf16) mma_bf16(dcol, adesc, bdesc, idesc, acc);
+                            if constexpr (C::kRouterAll) {
+                                const int nt = args.a_tiles > 0 ? args.a_tiles : 1;
+                                for (int t = 0; t < nt; ++t)
+                                    mma_bf16(dcol + t * BN, sdesc_sw128(abase + t * kATileBytes + k * 32), bdesc, idesc, acc);
+                            } else if constexpr (C::kBf16) mma_bf16(dcol, adesc, bdesc, idesc, acc);
                             else if constexpr (C::kTM) mma_f8(dcol, bdesc, adesc, idesc, acc);
                             else mma_f8(dcol, adesc, bdesc, idesc, acc);
                             if constexpr (C::kATiles == 2 && !C::kTM)
@@ -1107,20 +1126,23 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
                 // Router: one accumulator per item (one K split)
                 if (!mbar_wait(smem_u32(&pfull[pbuf]), pphase, abort_flag, args.err, ERR_WAIT_PART_FULL)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tcol = t_lane + pbuf * C::kPartCols + col_base;
-                const int e = I.mb * kBM + quad * 32 + lane;
                 float *dst = args.logits + static_cast<size_t>(I.ks) * args.total_rows * args.n_valid;
+                const int nt = (C::kRouterAll && args.a_tiles > 0) ? args.a_tiles : 1;
+                for (int t = 0; t < nt; ++t) {
+                    const uint32_t tcol = t_lane + pbuf * C::kPartCols + t * BN + col_base;
+                    const int e = (nt > 1 ? t : I.mb) * kBM + quad * 32 + lane;
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c) {
-                    if (c * 16 < n_my) {
-                        float p0[16];
-                        tmem_ld16(tcol + c * 16, p0);
-                        tmem_wait_ld();
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        if (c * 16 < n_my) {
+                            float p0[16];
+                            tmem_ld16(tcol + c * 16, p0);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int j = c * 16 + i;
-                            if (j < n_my && e < args.n_valid)
-                                dst[static_cast<size_t>(I.row0 + col_base + j) * args.n_valid + e] = p0[i];
+                            for (int i = 0; i < 16; ++i) {
+                                const int j = c * 16 + i;
+                                if (j < n_my && e < args.n_valid)
+                                    dst[static_cast<size_t>(I.row0 + col_base + j) * args.n_valid + e] = p0[i];
+                            }
                         }
                     }
                 }

@@ -36,6 +36,17 @@ def test_toy_router(T):
     _check(shape, x, wg, b)
 
 
+# batches past 512 tokens: 128-token tiles; one, three (the last ragged) and four
+# 128-expert blocks of W_g, and the Kimi width
+@pytest.mark.parametrize("T,E,d", [(600, 32, 1024), (1000, 384, 1024), (777, 300, 512), (520, 512, 256),
+                                   (2048, 384, 7168)])
+def test_router_token_tiles(T, E, d):
+    shape = S.MoEShape(f"wide_router_{T}_{E}", T=T, d=d, E=E, topk=8, H=256)
+    x = S.gen_x(T, d, seed=T + E)
+    wg, b = S.gen_router(shape, seed=T + E)
+    _check(shape, x, wg, b)
+
+
 def test_kimi_router_decode_batch():
     shape = S.DECODE
     x = S.gen_x(shape.T, shape.d, seed=0)
