@@ -566,9 +566,8 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap &map_a, cons
             // full boxes count toward the transaction bytes, including rows and a
             // K block beyond the tensor, which the TMA unit fills with zeros
             uint32_t bytes = C::kKPS * (C::kATiles * kATileBytes + kActBoxHeights[box_i] * kKBytes);
-            if constexpr (C::kRouterAll) {
-                if (args.a_tiles > 0) bytes = args.a_tiles * kATileBytes + kActBoxHeights[box_i] * kKBytes;
-            }
+            if constexpr (C::kRouterAll)   // the weight blocks actually loaded: a_tiles, or one
+                bytes = (args.a_tiles > 0 ? args.a_tiles : 1) * kATileBytes + kActBoxHeights[box_i] * kKBytes;
             // gathering GateUp: lane i copies the tile's row i (one token's 128-byte K
             // block, eight 16-byte copies into its 128-byte-swizzled place); only the
             // weights come by TMA. Rows past the tile's end stay as they are: their
