@@ -91,6 +91,19 @@ def test_layer_tiled_equals_row_major(T, n_shared):
     assert torch.equal(y, yt)
 
 
+# few groups against 152 CTAs: the decode GEMMs' first-round prefetch guesses items of
+# groups that do not exist and must skip them; one 128-row block per group
+@pytest.mark.parametrize("E,k,n_sh,H,d,T", [(8, 2, 0, 128, 256, 3), (4, 4, 1, 128, 384, 5), (16, 8, 2, 384, 256, 2)])
+def test_layer_tiled_few_groups(E, k, n_sh, H, d, T):
+    shape = S.MoEShape(f"t_few{E}", T=T, d=d, E=E, topk=k, H=H, n_shared=n_sh)
+    inp = S.gen_moe_inputs(shape, seed=E + T, device=DEV)
+    y = moe.layer_forward(inp.x, inp.w_gate, inp.bias, inp.experts, moe.cfg_of(shape))
+    yt = moe.layer_forward(inp.x, inp.w_gate, inp.bias, _tiled(inp.experts), moe.cfg_of(shape, w_tiled=True))
+    torch.cuda.synchronize()
+    moe.check_device_error(DEV)
+    assert torch.equal(y, yt)
+
+
 def test_block_tiled_equals_row_major():
     shape = S.MoEShape("t_block", T=96, d=1024, E=32, topk=8, H=256)
     inp = S.gen_moe_inputs(shape, seed=5, device=DEV)
