@@ -29,6 +29,20 @@ def test_bf16_random_bit_exact(rows, cols):
     np.testing.assert_array_equal(st.T.view(np.uint32), so.view(np.uint32))
 
 
+# group counts that leave the last warp's run ragged (2,997 and 161,007 groups), the
+# second large enough that every warp takes two runs of eight groups
+@pytest.mark.parametrize("rows,cols", [(999, 384), (23001, 896)])
+@pytest.mark.parametrize("bf16", [True, False])
+def test_ragged_group_runs_bit_exact(rows, cols, bf16):
+    g = torch.Generator().manual_seed(rows + cols)
+    x = torch.randn(rows, cols, generator=g) * torch.rand(rows, 1, generator=g) * 4
+    x = x.to(torch.bfloat16) if bf16 else x
+    q, s = _run(x, transposed=True)
+    qo, so = O.quantize_1x128(x.float().numpy())
+    np.testing.assert_array_equal(q, qo)
+    np.testing.assert_array_equal(s.T.view(np.uint32), so.view(np.uint32))
+
+
 def test_fp32_special_groups_bit_exact():
     rows, cols = 8, 512
     x = torch.randn(rows, cols) * 3
